@@ -1,0 +1,20 @@
+"""CPU float64 oracle for exact softmax attention.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.  It shares no code with the
+CUDA path.
+"""
+
+from .attention import (  # noqa: F401
+    attention,
+    attention_band,
+    attention_head,
+    attention_rows,
+    combine_rows,
+    decode,
+    lse_merge,
+    partial,
+    split_partials,
+    tree_combine,
+    visible,
+)
