@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on B300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra] [--no-cpu-baseline] [--no-e2e]
+
+A "step" is one launch of the hot path on one batch of the workload: by default
+the causal prefill of B=4, Hq=Hkv=16, N=4096, d=128 (bf16 in, f32 accumulate,
+bf16 O + f32 LSE), whose TFLOP/s is the headline value.  The same line carries
+the split-KV decode workloads (million-token and batched GQA, GB/s of K/V) and
+the local-window prefill as sub-objects, each with its own roofline.
+
+Timing: W warm-up launches, then K launches bracketed by CUDA events on the
+launching stream with a device synchronise (and, for N > 1, a barrier) on both
+sides; the max over ranks is taken.  Every workload's inputs exceed the 126 MB
+L2 (said in ``config.l2``), so no flush runs between launches.  SM clocks and
+throttle reasons are polled through NVML during the timed region.
+
+``--impl reference`` times the float64 CPU oracle (the deliberately slow
+reference of this repository) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s & decode KV GB/s on 1 B300, as % of roofline"
+PKG = "exact_transformer_attention_flashattention_b300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NAMEPLATE_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="causal_prefill_4k")
+    ap.add_argument("--no-extra", action="store_true", help="skip the decode/window sub-objects")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    """Hash of the kernel sources; a stored ncu traffic figure is used only if
+    it was taken from the same sources."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, PKG, "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rows = json.load(f)
+    except (OSError, ValueError):
+        return None
+    sha = kernel_source_sha()
+    for r in rows:
+        if r.get("kernel") == kernel and r.get("workload") == workload and r.get("source_sha") == sha:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+# ----------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self, gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Polls SM clock and clock-event (throttle) reasons through NVML from a
+    background thread; ``window`` marks the timed region and the summary uses
+    the samples taken inside it (all samples if the region was too short)."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, device_index: int):
+        self.ok = False
+        self.samples = []  # (time, sm_mhz, reasons)
+        self.t0 = self.t1 = None
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.get_reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except Exception as e:  # no NVML: clocks are reported as null
+            self.error = repr(e)
+
+    def _poll(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+            except Exception:
+                mhz = None
+            try:
+                rs = self.get_reasons(self.h)
+            except Exception:
+                rs = 0
+            if mhz is not None:
+                self.samples.append((time.perf_counter(), mhz, rs))
+            time.sleep(0.0005)
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        inside = [s for s in self.samples
+                  if self.t0 is not None and self.t0 <= s[0] <= self.t1]
+        use = inside or self.samples
+        bits = 0
+        for s in use:
+            bits |= s[2]
+        names = [n for n, bit in self.REASONS.items() if bits & bit and n != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(s[1] for s in use)),
+                "sm_max_mhz": self.max_mhz, "samples": len(use),
+                "in_timed_region": bool(inside), "reasons": names, "source": "NVML"}
+
+
+# ----------------------------------------------------------------- timing
+def time_launches(fn, steps: int, warmup: int, dist: Dist, clocks=None):
+    """Average device time of one call of ``fn`` (ms), CUDA events on the
+    current stream, max over ranks."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record()
+    for _ in range(steps):
+        fn()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if clocks is not None:
+        clocks.window(t0, t1)
+    dist.barrier()
+    return dist.max(start.elapsed_time(end) / steps)
+
+
+def roofline(achieved, peak, unit, bound, traffic, per_launch_units, unit_name):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_per_launch": per_launch_units, "algorithmic_unit": unit_name}
+
+
+# ----------------------------------------------------------------- workloads
+def prefill_case(w, dev):
+    import torch
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
+    q, k, v = (t.to(dev) for t in prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed))
+    o = torch.empty(w.B, w.N, w.Hq, w.d, dtype=torch.float32 if w.o_fp32 else torch.bfloat16,
+                    device=dev)
+    lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    return q, k, v, o, lse
+
+
+def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_flops
+    q, k, v, o, lse = prefill_case(w, "cuda")
+    flops = prefill_flops(w.B, w.Hq, w.N, w.d, w.causal, w.window)
+
+    def step():
+        fa.attn_fwd(q, k, v, causal=w.causal, window=w.window, scale=w.scale, out=o, lse=lse)
+
+    if clocks is not None:
+        with clocks:
+            ms = time_launches(step, steps, warmup, dist, clocks)
+    else:
+        ms = time_launches(step, steps, warmup, dist)
+    assert fa.device_status() == 0, fa.last_error()
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    rf = roofline(tflops, peak, "TFLOP/s", "tensor",
+                  stored_traffic("prefill_kernel", w.name), flops, "FLOP")
+    rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
+    rf["frac_of_sustained"] = round(tflops / peaks.get("bf16_tflops_sustained", peak), 4)
+    io_bytes = (q.numel() + k.numel() + v.numel()) * 2 + o.numel() * o.element_size() + lse.numel() * 4
+    return {"ms": ms, "tflops": tflops, "flops": flops, "roofline": rf, "io_bytes": io_bytes,
+            "launches_per_step": 1}
+
+
+def decode_case(w, dev):
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import decode_inputs
+    q, kc, vc, kv_len = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo,
+                                      w.kv_len_hi)
+    ws = torch.empty(fa.attn_decode_workspace_size(w.B, w.Hq, w.num_splits, w.d),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty(w.B, w.Hq, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.Hq, dtype=torch.float32, device=dev)
+    return q.to(dev), kc.to(dev), vc.to(dev), kv_len, kv_len.to(dev), ws, o, lse
+
+
+def bench_decode(w, steps, warmup, dist, peaks, peak_kind):
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import decode_kv_bytes
+    q, kc, vc, kv_len_host, kv_len, ws, o, lse = decode_case(w, "cuda")
+    kv_bytes = decode_kv_bytes(kv_len_host, w.Hkv, w.d)
+    m, l, po = fa.split_partials_view(ws, w.B, w.Hq, w.num_splits, w.d)
+
+    def full():
+        fa.attn_decode_splitkv(q, kc, vc, kv_len, w.num_splits, scale=w.scale, out=o, lse=lse,
+                               workspace=ws)
+
+    def partials():
+        fa.attn_decode_partials(q, kc, vc, kv_len, w.num_splits, scale=w.scale, workspace=ws)
+
+    def combine():
+        fa.lse_tree_combine(m, l, po, out=o, lse=lse)
+
+    ms_full = time_launches(full, steps, warmup, dist)
+    ms_part = time_launches(partials, steps, warmup, dist)
+    ms_comb = time_launches(combine, steps, warmup, dist)
+    assert fa.device_status() == 0, fa.last_error()
+    gbs = kv_bytes / (ms_full * 1e-3) / 1e9
+    part_gbs = kv_bytes / (ms_part * 1e-3) / 1e9
+    rf = roofline(part_gbs, peaks["hbm_gbs"], "GB/s", "hbm",
+                  stored_traffic("decode_partial_kernel", w.name), kv_bytes, "bytes of K/V")
+    rf["kernel"] = "decode_partial_kernel"
+    rf["peak_kind"] = f"{peak_kind} HBM copy"
+    rf["frac_of_nameplate_8tbs"] = round(part_gbs / NAMEPLATE_HBM_GBS, 4)
+    return {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": ms_full,
+            "kv_bytes": kv_bytes, "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+            "frac_of_nameplate_8tbs": round(gbs / NAMEPLATE_HBM_GBS, 4),
+            "kernels": {"decode_partial_kernel_ms": ms_part, "lse_combine_kernel_ms": ms_comb},
+            "launches_per_call": 2, "roofline": rf,
+            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lmax": w.N, "d": w.d,
+                       "num_splits": w.num_splits,
+                       "kv_len": "uniform [%d, %d]" % (w.kv_len_lo, w.kv_len_hi)
+                       if w.kv_len_lo else "full"}}
+
+
+def e2e_prefill(w, steps, dist):
+    """Through the public API with host buffers: pinned host -> device copies
+    of q, k, v, the prefill launch, device -> pinned host copies of O and LSE."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import (prefill_flops,
+                                                                        prefill_inputs)
+    qh, kh, vh = (t.pin_memory() for t in prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed))
+    oh = torch.empty(w.B, w.N, w.Hq, w.d, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device="cuda") for t in (qh, kh, vh))
+    od = torch.empty_like(oh, device="cuda")
+    ld = torch.empty_like(lh, device="cuda")
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa.attn_fwd(qd, kd, vd, causal=w.causal, window=w.window, scale=w.scale, out=od, lse=ld)
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(ld, non_blocking=True)
+
+    ms = time_launches(step, steps, 2, dist)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * 2 + lh.numel() * 4
+    flops = prefill_flops(w.B, w.Hq, w.N, w.d, w.causal, w.window) * dist.world
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_prefill_sample(w, rows_per_head: int, heads, inputs=None):
+    """Time the float64 oracle on `heads` (b, h) pairs, `rows_per_head` query
+    rows each (rows taken from the end, the most expensive causal rows).
+    Returns (seconds, algorithmic flops of the sampled rows)."""
+    import numpy as np
+    import oracle
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
+    q, k, v = inputs if inputs is not None else prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+    rows = np.arange(w.N - rows_per_head, w.N)
+    vis = oracle.visible(w.N, w.N, w.causal, w.window)[rows]
+    flops = 4.0 * w.d * float(vis.sum()) * len(heads)
+    t0 = time.perf_counter()
+    for b, h in heads:
+        oracle.attention_rows(q, k, v, b, h, rows, causal=w.causal, window=w.window,
+                              scale=w.scale)
+    return time.perf_counter() - t0, flops
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else None
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, budget_s: float):
+    """The oracle as it stands on the host cores: whole heads of the workload
+    until about `budget_s` seconds of work."""
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
+    inputs = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+    heads, secs, flops = [], 0.0, 0.0
+    i = 0
+    while secs < budget_s and i < w.B * w.Hq:
+        hd = [(i % w.B, (i * 7) % w.Hq)]
+        s, f = oracle_prefill_sample(w, w.N, hd, inputs)
+        secs, flops = secs + s, flops + f
+        heads += hd
+        i += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": blas_threads() or len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{len(heads)} of {w.B * w.Hq} (batch, head) pairs of {w.name}, all "
+                      f"{w.N} query rows each, float64 NumPy ({secs:.1f} s)",
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+def run_reference(args, w, dist):
+    """--impl reference: the oracle timed on bounded samples of the workload."""
+    if dist.rank != 0:
+        return
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
+    inputs = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+    budget = 150.0  # seconds for the whole --warmup + --steps run
+    # calibrate the rows per step so that (W + K) steps fit the budget
+    t, _ = oracle_prefill_sample(w, 256, [(0, 0)], inputs)
+    per_row = t / 256
+    rows = int(max(16, min(w.N, budget / max(1, args.steps + args.warmup) / per_row)))
+    for i in range(args.warmup):
+        oracle_prefill_sample(w, rows, [(i % w.B, i % w.Hq)], inputs)
+    secs = flops = 0.0
+    for i in range(args.steps):
+        s, f = oracle_prefill_sample(w, rows, [(i % w.B, (3 * i) % w.Hq)], inputs)
+        secs, flops = secs + s, flops + f
+    value = flops / secs / 1e12
+    cores = blas_threads() or len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"per step: the last {rows} query rows of one (batch, "
+                                       f"head) pair of {w.name}, float64 NumPy"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+           "causal": w.causal, "window": w.window, "scale": "1/sqrt(d)",
+           "o_dtype": "f32" if w.o_fp32 else "bf16", "inputs": "bf16 i.i.d. N(0,1), seeded"}
+    qkv = w.B * w.N * (w.Hq + 2 * w.Hkv) * w.d * 2
+    cfg["l2"] = f"inputs larger than L2 ({qkv / 2**20:.0f} MiB of Q/K/V vs 126 MB); no flush"
+    return cfg
+
+
+def main():
+    args = parse_args()
+    from exact_transformer_attention_flashattention_b300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    dist = Dist(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, w, dist)
+        dist.close()
+        return
+
+    import torch
+    torch.cuda.set_device(dist.local)
+    from exact_transformer_attention_flashattention_b300 import binding  # noqa: F401 (loads .so)
+    peaks, peak_kind = load_peaks()
+    if w.kind != "prefill":
+        raise SystemExit("the headline workload must be a prefill workload")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    main_res = bench_prefill(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
+    value = main_res["flops"] * dist.world / (main_res["ms"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(main_res["ms"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "roofline": main_res["roofline"], "gpu_launches": args.steps * main_res["launches_per_step"],
+        "clocks": clocks.summary(),
+    }
+    line["config"]["parallelism"] = f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
+    if not args.no_e2e:
+        line["e2e"] = e2e_prefill(w, max(3, min(args.steps, 10)), dist)
+    if not args.no_extra:
+        extra = {}
+        for name in ("decode_1m", "gqa_decode_batch32"):
+            extra[name] = bench_decode(WORKLOADS[name], max(3, min(args.steps, 50)),
+                                       max(3, args.warmup), dist, peaks, peak_kind)
+        wn = WORKLOADS["window_encoder_8k"]
+        r = bench_prefill(wn, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks,
+                          peak_kind)
+        extra["window_encoder_8k"] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
+                                      "ms_per_call": r["ms"], "roofline": r["roofline"],
+                                      "config": workload_config(wn)}
+        line["extra"] = extra
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

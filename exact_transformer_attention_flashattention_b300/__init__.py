@@ -1,0 +1,24 @@
+"""Exact softmax attention for NVIDIA B300 (sm_103a).
+
+Prefill (causal, sliding-window, non-causal) and split-KV decode with a
+logsumexp tree combine, implemented as hand-written CUDA behind the C ABI of
+include/b300attn.h.  The compute entry points are re-exported lazily from
+``binding`` so that ``inputs`` can be imported on machines without the built
+library; touching any entry point loads libb300attn.so and fails loudly if it
+is missing.
+"""
+
+_BINDING = {
+    "attn_fwd", "attn_decode_splitkv", "attn_decode_partials", "lse_tree_combine", "attn_decode_chunk",
+    "attn_decode_workspace_size", "device_status", "last_error", "split_partials_view",
+    "B300AttnError", "lib", "LIB_PATH",
+}
+
+__all__ = sorted(_BINDING)
+
+
+def __getattr__(name):
+    if name in _BINDING:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

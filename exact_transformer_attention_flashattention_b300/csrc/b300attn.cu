@@ -1,0 +1,341 @@
+// C ABI of the b300attn library: argument validation, TMA tensor-map encoding,
+// launch configuration.  All kernels live in this translation unit so that
+// their status words can be read back by attn_device_status.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "b300attn.h"
+#include "decode.cuh"
+#include "prefill.cuh"
+
+using namespace b300;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(B300ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map over a row-major [d3][d2][d1][d0] array (d0 contiguous).
+int make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t d3, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3,
+                CUtensorMapSwizzle swizzle, const char* name) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {b0, b1, b2, b3};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                static_cast<int>(r));
+  return B300ATTN_OK;
+}
+
+template <typename K>
+int set_smem(K kernel, int bytes) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  return B300ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+template <int D>
+int launch_prefill(const void* q, const void* k, const void* v, const PrefillParams& p,
+                   cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map_4d(&tq, q, D, p.Hq, p.N, p.B, 64, 1, C::BM, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tk, k, D, p.Hkv, p.N, p.B, 64, 1, C::BN, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tv, v, D, p.Hkv, p.N, p.B, 64, 1, C::BN, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
+    return rc;
+  if ((rc = set_smem(prefill_kernel<D>, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
+  const long long grid = static_cast<long long>(p.nqb) * p.Hq * p.B;
+  prefill_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk,
+                                                                                       tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return B300ATTN_OK;
+}
+
+template <int D, int GT>
+int launch_decode(const void* k_cache, const void* v_cache, const DecodeParams& p,
+                  cudaStream_t stream) {
+  using L = DecSmem<D, GT>;
+  CUtensorMap tk, tv;
+  int rc;
+  if ((rc = make_map_4d(&tk, k_cache, D, p.Hkv, p.Lmax, p.B, D, 1, kDecSub, 1,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, "k_cache")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tv, v_cache, D, p.Hkv, p.Lmax, p.B, D, 1, kDecSub, 1,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache")) != B300ATTN_OK)
+    return rc;
+  if ((rc = set_smem(decode_partial_kernel<D, GT>, L::BYTES)) != B300ATTN_OK) return rc;
+  const dim3 grid(p.S, p.Hkv * (p.G / GT), p.B);
+  decode_partial_kernel<D, GT><<<grid, kDecThreads, L::BYTES, stream>>>(tk, tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return B300ATTN_OK;
+}
+
+template <int D>
+int launch_decode_gt(int GT, const void* kc, const void* vc, const DecodeParams& p,
+                     cudaStream_t s) {
+  switch (GT) {
+    case 8: return launch_decode<D, 8>(kc, vc, p, s);
+    case 4: return launch_decode<D, 4>(kc, vc, p, s);
+    case 2: return launch_decode<D, 2>(kc, vc, p, s);
+    default: return launch_decode<D, 1>(kc, vc, p, s);
+  }
+}
+
+int launch_combine(const float* pm, const float* pl, const float* po, void* o, float* lse,
+                   int rows, int S, int d, int o_f32, cudaStream_t stream) {
+  const dim3 grid(rows, d / 32);
+  if (S > 64) {
+    if (d == 128)
+      lse_combine_kernel<128, 32><<<grid, 1024, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
+    else
+      lse_combine_kernel<64, 32><<<grid, 1024, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
+  } else {
+    if (d == 128)
+      lse_combine_kernel<128, 4><<<grid, 128, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
+    else
+      lse_combine_kernel<64, 4><<<grid, 128, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return B300ATTN_OK;
+}
+
+int check_common(int d, int o_dtype) {
+  if (d != 64 && d != 128)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "head dimension d=%d is not supported (64 or 128)", d);
+  if (o_dtype != B300ATTN_BF16 && o_dtype != B300ATTN_F32)
+    return fail(B300ATTN_ERR_INVALID, "o_dtype=%d must be 0 (bf16) or 1 (f32)", o_dtype);
+  return B300ATTN_OK;
+}
+
+// Validates the decode arguments shared by attn_decode_partials and
+// attn_decode_splitkv and fills `p`; returns B300ATTN_OK with p.B == 0 when
+// there is nothing to compute.
+int decode_setup(const void* q, const void* k_cache, const void* v_cache, const int* kv_len,
+                 int B, int Hq, int Hkv, int max_kv_len, int d, float scale, int num_splits,
+                 void* workspace, size_t workspace_bytes, DecodeParams& p, int& GT) {
+  p.B = 0;
+  if (B < 0 || Hq < 0 || Hkv < 0 || d < 0 || max_kv_len < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size");
+  if (B == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  int rc = check_common(d, B300ATTN_BF16);
+  if (rc != B300ATTN_OK) return rc;
+  if (max_kv_len < 1) return fail(B300ATTN_ERR_INVALID, "max_kv_len must be >= 1");
+  if (num_splits < 1 || num_splits > 65535)
+    return fail(B300ATTN_ERR_INVALID, "num_splits=%d must be in [1, 65535]", num_splits);
+  if (B > 65535) return fail(B300ATTN_ERR_UNSUPPORTED, "B=%d > 65535", B);
+  if (!q || !k_cache || !v_cache || !kv_len)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0");
+  const size_t need = attn_decode_workspace_size(B, Hq, num_splits, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(B300ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : static_cast<size_t>(0));
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(B300ATTN_ERR_INVALID, "workspace must be 256-byte aligned");
+  const int G = Hq / Hkv;
+  GT = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  if (static_cast<long long>(Hkv) * (G / GT) > 65535)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "too many heads for one launch");
+
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kv_len = kv_len;
+  p.part_m = static_cast<float*>(workspace);
+  p.part_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * 4));
+  p.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * align256(rows * 4));
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lmax = max_kv_len;
+  p.chunk = attn_decode_chunk(max_kv_len, num_splits);
+  p.S = num_splits;
+  p.G = G;
+  p.scale_log2 = scale * kLog2e;
+  return B300ATTN_OK;
+}
+
+int launch_partials(int d, int GT, const void* k_cache, const void* v_cache,
+                    const DecodeParams& p, cudaStream_t stream) {
+  return d == 128 ? launch_decode_gt<128>(GT, k_cache, v_cache, p, stream)
+                  : launch_decode_gt<64>(GT, k_cache, v_cache, p, stream);
+}
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_last_error(void) { return g_last_error.c_str(); }
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int d, int causal, int window, float scale, cudaStream_t stream,
+             int o_dtype) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size (B=%d Hq=%d Hkv=%d N=%d d=%d)", B, Hq, Hkv,
+                N, d);
+  if (B == 0 || N == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (causal != 0 && causal != 1) return fail(B300ATTN_ERR_INVALID, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
+                static_cast<double>(scale));
+  PrefillParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.window = window < 0 ? -1 : window;
+  p.o_f32 = o_dtype == B300ATTN_F32;
+  p.nqb = (N + 255) / 256;
+  // a zero scale is kept strictly positive so that masked (-inf) scores stay -inf
+  p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
+  const long long grid = static_cast<long long>(p.nqb) * Hq * B;
+  if (grid > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "grid too large");
+  return d == 128 ? launch_prefill<128>(q, k, v, p, stream) : launch_prefill<64>(q, k, v, p, stream);
+}
+
+int attn_decode_chunk(int max_kv_len, int num_splits) {
+  if (max_kv_len < 1 || num_splits < 1)
+    return fail(B300ATTN_ERR_INVALID, "max_kv_len=%d and num_splits=%d must be >= 1", max_kv_len,
+                num_splits);
+  const long long c = (static_cast<long long>(max_kv_len) + num_splits - 1) / num_splits;
+  return static_cast<int>((c + kDecSub - 1) / kDecSub * kDecSub);
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int num_splits, int d) {
+  if (B < 0 || Hq < 0 || num_splits < 1 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
+  return 2 * align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
+
+
+int attn_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                         const int* kv_len, int B, int Hq, int Hkv, int max_kv_len, int d,
+                         float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  DecodeParams p;
+  int GT = 1;
+  int rc = decode_setup(q, k_cache, v_cache, kv_len, B, Hq, Hkv, max_kv_len, d, scale,
+                        num_splits, workspace, workspace_bytes, p, GT);
+  if (rc != B300ATTN_OK || p.B == 0) return rc;
+  return launch_partials(d, GT, k_cache, v_cache, p, stream);
+}
+
+int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                        const int* kv_len, void* o, float* lse, int B, int Hq, int Hkv,
+                        int max_kv_len, int d, float scale, int num_splits, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream, int o_dtype) {
+  DecodeParams p;
+  int GT = 1;
+  int rc = decode_setup(q, k_cache, v_cache, kv_len, B, Hq, Hkv, max_kv_len, d, scale,
+                        num_splits, workspace, workspace_bytes, p, GT);
+  if (rc != B300ATTN_OK || p.B == 0) return rc;
+  if ((rc = check_common(d, o_dtype)) != B300ATTN_OK) return rc;
+  if (!o || !lse) return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(o) || !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if ((rc = launch_partials(d, GT, k_cache, v_cache, p, stream)) != B300ATTN_OK) return rc;
+  return launch_combine(p.part_m, p.part_l, p.part_o, o, lse, B * Hq, num_splits, d,
+                        o_dtype == B300ATTN_F32, stream);
+}
+
+int lse_tree_combine(const float* part_m, const float* part_l, const float* part_o, void* o,
+                     float* lse, int rows, int num_splits, int d, cudaStream_t stream,
+                     int o_dtype) {
+  if (rows < 0 || d < 0) return fail(B300ATTN_ERR_INVALID, "negative size");
+  if (rows == 0) return B300ATTN_OK;
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (num_splits < 1) return fail(B300ATTN_ERR_INVALID, "num_splits must be >= 1");
+  if (!part_m || !part_l || !part_o || !o || !lse)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  return launch_combine(part_m, part_l, part_o, o, lse, rows, num_splits, d,
+                        o_dtype == B300ATTN_F32, stream);
+}
+
+int attn_device_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int a = 0, b = 0;
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpyFromSymbol(&a, g_prefill_status, sizeof(a))) != cudaSuccess ||
+      (e = cudaMemcpyFromSymbol(&b, g_decode_status, sizeof(b))) != cudaSuccess)
+    return cuda_fail(e, "reading the device status word");
+  if (a | b) {
+    cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
+    cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));
+    return fail(B300ATTN_ERR_TIMEOUT,
+                "a kernel gave up on a bounded wait (status bits prefill=0x%x decode=0x%x)", a, b);
+  }
+  return B300ATTN_OK;
+}
+
+}  // extern "C"

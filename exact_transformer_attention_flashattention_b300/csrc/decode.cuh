@@ -1,0 +1,408 @@
+// Split-KV single-query decode and the logsumexp tree combine, sm_103a.
+//
+// The key axis of every sequence is cut into chunks; one CTA per (sequence,
+// kv head, chunk) computes, for every query head of the GQA group, the
+// partial triple over its keys
+//     m = max_j s_j,  l = sum_j 2^(s_j - m),  o = sum_j 2^(s_j - m) v_j
+// (scores in base-2 units inside the kernel; m is stored in natural-log
+// units).  A second kernel merges the triples of a row with the associative
+//     (m,l,o) + (m',l',o') = (M, l 2^(m-M) + l' 2^(m'-M), o 2^(m-M) + o' 2^(m'-M))
+// in a tree.  Source: "Tree Attention: Topology-aware Decoding for
+// Long-Context Attention on GPU Clusters" (express24.ir), abstract -- the
+// reduction across the sequence axis is associative and parallel as a tree;
+// here the tree runs inside one GPU.
+//
+// The decode path is bound by HBM bandwidth: each K/V byte is read once for
+// the whole GQA group (the inter-head packing idea of "FlashAttention for
+// Scalable Vector Architectures", gist.science), staged by TMA into a shared
+// memory ring, and read back with 128-bit loads.  Dot products run on CUDA
+// cores with a butterfly reduce-scatter across the lanes that share a key.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace b300 {
+
+__device__ unsigned int g_decode_status;
+
+constexpr unsigned kStatusDecodeProducer = 8u, kStatusDecodeConsumer = 16u;
+
+constexpr int kDecSub = 64;      // keys per ring stage
+constexpr int kDecCWarps = 4;    // consumer warps (16 keys of each stage each)
+constexpr int kDecThreads = 160; // + one producer warp
+
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [B, Hq, D]
+  const int* kv_len;       // [B]
+  float* part_m;           // [B*Hq, S]   natural-log units
+  float* part_l;           // [B*Hq, S]
+  float* part_o;           // [B*Hq, S, D]
+  int B, Hq, Hkv, Lmax, chunk, S, G;
+  float scale_log2;
+};
+
+template <int D>
+struct DecCfg {
+  static constexpr int STAGES = (D == 128) ? 3 : 6;
+  static constexpr int HALF_BYTES = kDecSub * D * 2;  // K (or V) rows of one stage
+  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
+  static constexpr int LPK = D / 8;          // lanes that share one key row (16 B each)
+  static constexpr int NG = 32 / LPK;        // key groups per warp
+  static constexpr int KPG = 16 / NG;        // keys per group per stage
+  static constexpr int STEPS = (LPK == 16) ? 4 : 3;  // log2(LPK)
+};
+
+template <int D, int GT>
+struct DecSmem {
+  static constexpr int RING = DecCfg<D>::STAGES * DecCfg<D>::STAGE_BYTES;
+  static constexpr int SCORES = kDecCWarps * 16 * GT * 4;            // per-warp s / p
+  static constexpr int MERGE_O = kDecCWarps * GT * D * 4;            // per-warp o
+  static constexpr int MERGE_ML = 2 * kDecCWarps * GT * 4;           // per-warp m, l
+  static constexpr int BARS = 2 * DecCfg<D>::STAGES * 8;
+  static constexpr int OFF_SCORES = RING;
+  static constexpr int OFF_MO = OFF_SCORES + SCORES;
+  static constexpr int OFF_ML = OFF_MO + MERGE_O;
+  static constexpr int OFF_BARS = (OFF_ML + MERGE_ML + 15) & ~15;
+  static constexpr int BYTES = OFF_BARS + BARS + 128;  // + alignment slack
+};
+
+// One CTA: (split = blockIdx.x, kv head x head group = blockIdx.y, sequence = blockIdx.z).
+// GT query heads per CTA (the whole GQA group when it is 1, 2, 4 or 8 heads).
+template <int D, int GT>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  using C = DecCfg<D>;
+  using L = DecSmem<D, GT>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int LPK = C::LPK, KPG = C::KPG;
+  constexpr int VAL = KPG * GT;  // partial dot products per lane before the reduce-scatter
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  float* s_sm = reinterpret_cast<float*>(smem + L::OFF_SCORES);
+  float* mo_sm = reinterpret_cast<float*>(smem + L::OFF_MO);
+  float* mm_sm = reinterpret_cast<float*>(smem + L::OFF_ML);
+  float* ml_sm = mm_sm + kDecCWarps * GT;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
+  uint64_t* empty = full + STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int ngroups = p.G / GT;
+  const int hkv = blockIdx.y / ngroups;
+  const int hq0 = hkv * p.G + (blockIdx.y % ngroups) * GT;
+  const int b = blockIdx.z;
+
+  int len = p.kv_len[b];
+  len = min(max(len, 0), p.Lmax);
+  const int key0 = split * p.chunk;
+  const int nkeys = min(max(len - key0, 0), p.chunk);
+  const int nsub = (nkeys + kDecSub - 1) / kDecSub;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecCWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kDecCWarps) {
+    // ================================================================ producer
+    if (lane == 0 && nsub > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int issued = 0;
+      for (; issued < nsub; ++issued) {
+        const int s = issued % STAGES;
+        if (issued >= STAGES &&
+            !mbar_wait(&empty[s], ((issued / STAGES) - 1) & 1, &g_decode_status,
+                       kStatusDecodeProducer))
+          break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        uint8_t* dst = smem + s * C::STAGE_BYTES;
+        tma_load_4d(dst, &tm_k, &full[s], 0, hkv, key0 + issued * kDecSub, b);
+        tma_load_4d(dst + C::HALF_BYTES, &tm_v, &full[s], 0, hkv, key0 + issued * kDecSub, b);
+      }
+      for (int u = max(0, issued - STAGES); u < issued; ++u)
+        mbar_wait(&full[u % STAGES], (u / STAGES) & 1, &g_decode_status, kStatusDecodeProducer);
+    }
+    return;  // the producer takes no part in the merge below
+  }
+
+  // ================================================================ consumers
+  const int grp = lane / LPK;  // key group within the warp
+  const int li = lane % LPK;   // 8 consecutive elements of d: [8*li, 8*li+8)
+  float* s_w = s_sm + warp * 16 * GT;
+
+  float qf[GT][8];  // q * scale * log2(e), this lane's slice of d
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    const uint4 w = *reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(b) * p.Hq + hq0 + g) * D + 8 * li);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[g][2 * e] = bf16lo_to_f32(u[e]) * p.scale_log2;
+      qf[g][2 * e + 1] = bf16hi_to_f32(u[e]) * p.scale_log2;
+    }
+  }
+  float acc[GT][8];
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+  float m_ref[GT];  // base-2 running maximum per head (warp-uniform)
+#pragma unroll
+  for (int g = 0; g < GT; ++g) m_ref[g] = -INFINITY;
+  float lsum = 0.f;  // this lane's share of l for head (lane % GT)
+
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int stage = sub % STAGES;
+    bool ok = mbar_wait(&full[stage], (sub / STAGES) & 1, &g_decode_status, kStatusDecodeConsumer);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const uint8_t* Ks = smem + stage * C::STAGE_BYTES;
+    const uint8_t* Vs = Ks + C::HALF_BYTES;
+    const int nvalid = min(kDecSub, nkeys - sub * kDecSub);
+    const int wkey0 = warp * 16;  // this warp's 16 keys of the stage
+
+    // ---- s = q . k for KPG keys x GT heads, partial over this lane's 8 elements
+    float val[VAL];
+#pragma unroll
+    for (int kk = 0; kk < KPG; ++kk) {
+      const int key = wkey0 + grp * KPG + kk;
+      const uint4 w = *reinterpret_cast<const uint4*>(Ks + key * (D * 2) + li * 16);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+      float kf[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kf[2 * e] = bf16lo_to_f32(u[e]);
+        kf[2 * e + 1] = bf16hi_to_f32(u[e]);
+      }
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+        val[kk * GT + g] = a;
+      }
+    }
+    // ---- butterfly reduce-scatter over the LPK lanes of the group
+    int base = 0;
+#pragma unroll
+    for (int st = 0, cur = VAL; st < C::STEPS; ++st) {
+      const int mask = LPK >> (st + 1);
+      if (cur >= 2) {
+        const int half = cur / 2;
+        const bool up = (lane & mask) != 0;
+#pragma unroll
+        for (int v = 0; v < VAL / 2; ++v) {
+          if (v < half) {
+            const float send = up ? val[v] : val[v + half];
+            const float keep = up ? val[v + half] : val[v];
+            val[v] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        }
+        if (up) base += half;
+        cur = half;
+      } else {
+        val[0] += __shfl_xor_sync(0xffffffffu, val[0], mask);
+      }
+    }
+    constexpr int FINAL = (VAL >= LPK) ? VAL / LPK : 1;
+#pragma unroll
+    for (int v = 0; v < FINAL; ++v) {
+      const int idx = base + v;  // = key_in_group * GT + head
+      s_w[(grp * KPG + idx / GT) * GT + idx % GT] = val[v];
+    }
+    __syncwarp();
+
+    // ---- online softmax over the warp's 16 keys x GT heads
+    constexpr int NV = (16 * GT + 31) / 32;
+    const int myg = lane % GT;
+    float x[NV];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+      const int v = lane + 32 * t;
+      x[t] = -INFINITY;
+      if (v < 16 * GT && wkey0 + v / GT < nvalid) x[t] = s_w[v];
+      mx = fmaxf(mx, x[t]);
+    }
+#pragma unroll
+    for (int mask = GT; mask < 32; mask <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+    float mu_mine = 0.f;
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      const float mn = fmaxf(m_ref[g], __shfl_sync(0xffffffffu, mx, g));
+      if (mn > m_ref[g] + kRescaleThreshold) {  // warp-uniform
+        const float alpha = ex2_approx(m_ref[g] - mn);
+        m_ref[g] = mn;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        if (myg == g) lsum *= alpha;
+      }
+      if (myg == g) mu_mine = (m_ref[g] == -INFINITY) ? 0.f : m_ref[g];
+    }
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+      const int v = lane + 32 * t;
+      const float pv = ex2_approx(x[t] - mu_mine);
+      lsum += pv;
+      if (v < 16 * GT) s_w[v] = pv;
+    }
+    __syncwarp();
+
+    // ---- o += p v over this group's keys
+#pragma unroll
+    for (int kk = 0; kk < KPG; ++kk) {
+      const int kl = grp * KPG + kk;
+      if (wkey0 + kl < nvalid) {
+        const uint4 w = *reinterpret_cast<const uint4*>(Vs + (wkey0 + kl) * (D * 2) + li * 16);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        float vf[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          vf[2 * e] = bf16lo_to_f32(u[e]);
+          vf[2 * e + 1] = bf16hi_to_f32(u[e]);
+        }
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          const float pg = s_w[kl * GT + g];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pg, vf[e], acc[g][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+  }
+
+  // ---- merge the key groups of the warp, then the four warps
+#pragma unroll
+  for (int mask = LPK; mask < 32; mask <<= 1) {
+#pragma unroll
+    for (int g = 0; g < GT; ++g)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], mask);
+  }
+#pragma unroll
+  for (int mask = GT; mask < 32; mask <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, mask);
+  if (lane < LPK) {
+#pragma unroll
+    for (int g = 0; g < GT; ++g)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mo_sm[(warp * GT + g) * D + 8 * lane + e] = acc[g][e];
+  }
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+    if (lane == g) {
+      mm_sm[warp * GT + g] = m_ref[g];
+      ml_sm[warp * GT + g] = lsum;
+    }
+  named_bar_sync(1, kDecCWarps * 32);
+  for (int idx = threadIdx.x; idx < GT * D; idx += kDecCWarps * 32) {
+    const int g = idx / D, dd = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecCWarps; ++w) M = fmaxf(M, mm_sm[w * GT + g]);
+    float o = 0.f, lt = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecCWarps; ++w) {
+        const float mw = mm_sm[w * GT + g];
+        if (mw != -INFINITY) {
+          const float c = ex2_approx(mw - M);
+          o = fmaf(mo_sm[(w * GT + g) * D + dd], c, o);
+          lt = fmaf(ml_sm[w * GT + g], c, lt);
+        }
+      }
+    }
+    const size_t prow = static_cast<size_t>(b) * p.Hq + hq0 + g;
+    p.part_o[(prow * p.S + split) * D + dd] = o;
+    if (dd == 0) {
+      p.part_m[prow * p.S + split] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+      p.part_l[prow * p.S + split] = lt;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tree combine: one CTA per (row, 32 columns of d) with NW warps (4 when there
+// are few splits, 32 when there are many).  Each warp folds a strided subset of
+// the partials (eight at a time, merged pairwise), then the NW warp results are
+// merged pairwise in log2(NW) levels through shared memory.
+// ---------------------------------------------------------------------------
+
+struct Triple {
+  float m, l, o;  // m in base-2 units
+};
+
+__device__ __forceinline__ Triple lse_merge(Triple a, Triple c) {
+  if (c.m == -INFINITY) return a;
+  if (a.m == -INFINITY) return c;
+  const float M = fmaxf(a.m, c.m);
+  const float wa = ex2_approx(a.m - M), wc = ex2_approx(c.m - M);
+  return Triple{M, fmaf(a.l, wa, c.l * wc), fmaf(a.o, wa, c.o * wc)};
+}
+
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32)
+    lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                       const float* __restrict__ po, void* out, float* lse, int S, int o_f32) {
+  __shared__ Triple red[NW][32];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.y * 32 + lane;
+  const float* mrow = pm + static_cast<size_t>(row) * S;
+  const float* lrow = pl + static_cast<size_t>(row) * S;
+  const float* orow = po + static_cast<size_t>(row) * S * D + col;
+
+  Triple acc{-INFINITY, 0.f, 0.f};
+  constexpr int BATCH = 8;
+  for (int s0 = warp; s0 < S; s0 += NW * BATCH) {
+    Triple t[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int s = s0 + u * NW;
+      t[u] = Triple{-INFINITY, 0.f, 0.f};
+      if (s < S) {
+        const float m = mrow[s];
+        t[u].m = (m == -INFINITY) ? -INFINITY : m * kLog2e;
+        if (t[u].m != -INFINITY) {
+          t[u].l = lrow[s];
+          t[u].o = orow[static_cast<size_t>(s) * D];
+        }
+      }
+    }
+#pragma unroll
+    for (int w = 1; w < BATCH; w <<= 1)
+#pragma unroll
+      for (int u = 0; u + w < BATCH; u += 2 * w) t[u] = lse_merge(t[u], t[u + w]);
+    acc = lse_merge(acc, t[0]);
+  }
+  red[warp][lane] = acc;
+  __syncthreads();
+#pragma unroll
+  for (int w = NW / 2; w >= 1; w >>= 1) {
+    if (warp < w) red[warp][lane] = lse_merge(red[warp][lane], red[warp + w][lane]);
+    __syncthreads();
+  }
+  if (warp == 0) {
+    const Triple r = red[0][lane];
+    const float val = (r.l > 0.f) ? r.o / r.l : 0.f;
+    const size_t oi = static_cast<size_t>(row) * D + col;
+    if (o_f32)
+      static_cast<float*>(out)[oi] = val;
+    else
+      static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(val);
+    if (blockIdx.y == 0 && lane == 0)
+      lse[row] = (r.l > 0.f) ? (r.m + __log2f(r.l)) * kLn2 : -INFINITY;
+  }
+}
+
+}  // namespace b300

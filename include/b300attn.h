@@ -1,0 +1,174 @@
+/*
+ * b300attn: exact softmax attention for NVIDIA B300 (sm_103a), C ABI.
+ *
+ *   O = softmax(scale * Q K^T + mask) V,   LSE_i = ln sum_j exp(scale * q_i.k_j + mask_ij)
+ *
+ * computed by tiling with an online softmax, so the N x N score matrix never
+ * reaches global memory ("FlashAttention" learn page, aiunderstanding.org,
+ * sections "Deep dive" and "Technical insight"; FAQ on exactness: the result
+ * is the same as standard attention, only the order of the work changes).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller.  The
+ *    library never allocates or frees memory and never synchronises the
+ *    stream; all work is enqueued on `stream` (0 = legacy default stream).
+ *  - Layouts are row-major with the head dimension d contiguous; bf16 means
+ *    IEEE bfloat16, f32 means IEEE binary32.
+ *  - Query head h reads key/value head h / (Hq / Hkv) (grouped-query heads).
+ *  - A row with no visible key gets O = 0 and LSE = -inf.
+ *  - Return value: B300ATTN_OK, or a negative b300attn_status.  On a host-side
+ *    error nothing is enqueued and attn_last_error() describes the problem.
+ *    B300ATTN_ERR_CUDA means a CUDA call (e.g. the launch) failed.
+ *  - Inputs with nothing to compute (B == 0, N == 0, rows == 0) return OK and
+ *    enqueue nothing; pointers may then be NULL.
+ *  - Thread safety: stateless apart from a thread-local error message and a
+ *    per-device status word written only when a kernel's bounded wait expires.
+ */
+#ifndef B300ATTN_H
+#define B300ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definition as the CUDA runtime's; passing a cudaStream_t works as is. */
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  B300ATTN_OK = 0,
+  B300ATTN_ERR_INVALID = -1,     /* bad argument: NULL, negative size, misaligned, ... */
+  B300ATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. d not in {64,128}) */
+  B300ATTN_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
+  B300ATTN_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed */
+  B300ATTN_ERR_TIMEOUT = -5      /* a kernel gave up on a bounded wait (see attn_device_status) */
+} b300attn_status;
+
+typedef enum { B300ATTN_BF16 = 0, B300ATTN_F32 = 1 } b300attn_dtype;
+
+/*
+ * attn_fwd -- prefill attention (causal, sliding-window or non-causal).
+ *
+ * Implements the tiled, online-softmax form of attention: Q, K, V move through
+ * on-chip memory in tiles, a running row maximum and row sum are kept and
+ * partial outputs rescaled as new tiles arrive ("FlashAttention" learn page,
+ * "Technical insight" and FAQ on how softmax is computed without seeing all
+ * scores); key tiles a row cannot see are skipped.  The window is the local
+ * attention of the Arabic thread on extending context length (point 1:
+ * tokens attend only to their neighbours).
+ *
+ *   q    bf16 [B, N, Hq,  d]       k, v  bf16 [B, N, Hkv, d]
+ *   o    [B, N, Hq, d], bf16 or f32 as o_dtype says
+ *   lse  f32  [B, Hq, N], natural logarithm
+ *   causal  0/1: row i sees keys j <= i (square, top-left aligned)
+ *   window  < 0: no window; w >= 0: row i sees keys with |i - j| <= w
+ *           (with causal: i - w <= j <= i)
+ *   scale   finite, >= 0 (1/sqrt(d) is the usual choice)
+ *   d in {64, 128}; Hq % Hkv == 0; every pointer 16-byte aligned.
+ * Errors: INVALID (NULL/negative/misaligned/bad scale or dtype), UNSUPPORTED (d),
+ * CUDA (launch failure).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int d, int causal, int window, float scale, cudaStream_t stream,
+             int o_dtype);
+
+/*
+ * attn_decode_chunk -- keys per split used by attn_decode_splitkv:
+ * ceil(max_kv_len / num_splits) rounded up to a multiple of 64.  Returns a
+ * negative status on invalid arguments.
+ */
+int attn_decode_chunk(int max_kv_len, int num_splits);
+
+/*
+ * attn_decode_workspace_size -- bytes of workspace attn_decode_splitkv needs
+ * for the split partials: f32 m and l [B, Hq, num_splits] and f32 o
+ * [B, Hq, num_splits, d], each region 256-byte aligned.  0 on invalid input.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int num_splits, int d);
+
+/*
+ * attn_decode_splitkv -- single-query decode over a (possibly ragged) KV cache.
+ *
+ * The key axis of every sequence is cut into num_splits chunks of
+ * attn_decode_chunk(max_kv_len, num_splits) keys.  One kernel computes, per
+ * (sequence, kv head, chunk), the partial triple of every query head in the
+ * group -- m = max score, l = sum exp(s - m), o = sum exp(s - m) v -- streaming
+ * each K/V byte once per group; a second kernel merges the partials with the
+ * logsumexp tree of lse_tree_combine.  The split and the tree follow the Tree
+ * Attention page (express24.ir), abstract: the reduction along the sequence
+ * axis is associative and can be computed as a tree.
+ *
+ *   q        bf16 [B, Hq, d]
+ *   k_cache, v_cache  bf16 [B, max_kv_len, Hkv, d]; only rows < kv_len[b] are read
+ *                     into the result (rows beyond may hold anything, even NaN)
+ *   kv_len   int32 [B], device; values are clamped to [0, max_kv_len]
+ *   o        [B, Hq, d] bf16 or f32 (o_dtype);  lse  f32 [B, Hq]
+ *   workspace  device buffer of at least attn_decode_workspace_size(B, Hq,
+ *              num_splits, d) bytes, 256-byte aligned; contents on return are
+ *              the partials (m in natural-log units).
+ *   d in {64, 128}; Hq % Hkv == 0; 1 <= num_splits <= 65535.
+ * Errors: INVALID, UNSUPPORTED, WORKSPACE (NULL or too small), CUDA.
+ */
+int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                        const int* kv_len, void* o, float* lse, int B, int Hq, int Hkv,
+                        int max_kv_len, int d, float scale, int num_splits, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream, int o_dtype);
+
+/*
+ * attn_decode_partials -- the first half of attn_decode_splitkv on its own:
+ * writes the per-split partial triples (m, l, o) of every query head into
+ * `workspace` (layout as described for attn_decode_splitkv) and does not merge
+ * them.  Partials produced on different devices or streams for disjoint key
+ * ranges can be merged with lse_tree_combine, which is the cross-device
+ * decoding scheme of the Tree Attention page (abstract).  Arguments as for
+ * attn_decode_splitkv, without o, lse and o_dtype.  Split c of sequence b
+ * covers keys [c*chunk, min((c+1)*chunk, kv_len[b])); an empty split gets
+ * m = -inf, l = 0, o = 0.
+ */
+int attn_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                         const int* kv_len, int B, int Hq, int Hkv, int max_kv_len, int d,
+                         float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * lse_tree_combine -- merge split partials in a logsumexp tree.
+ *
+ * For each of `rows` rows, merges num_splits triples (m, l, o) with
+ *   (m,l,o) + (m',l',o') = (M, l e^(m-M) + l' e^(m'-M), o e^(m-M) + o' e^(m'-M)),
+ *   M = max(m, m'),
+ * (Tree Attention page, abstract: the sequence-axis reduction as a tree), then
+ * writes O = o / l and LSE = M + ln l.  A partial with m = -inf is the empty
+ * identity and its o is never read.
+ *
+ *   part_m, part_l  f32 [rows, num_splits]   (m in natural-log units)
+ *   part_o          f32 [rows, num_splits, d]
+ *   o               [rows, d] bf16 or f32 (o_dtype);  lse  f32 [rows]
+ *   d in {64, 128}; num_splits >= 1.
+ * Errors: INVALID, UNSUPPORTED, CUDA.
+ */
+int lse_tree_combine(const float* part_m, const float* part_l, const float* part_o, void* o,
+                     float* lse, int rows, int num_splits, int d, cudaStream_t stream,
+                     int o_dtype);
+
+/*
+ * attn_device_status -- synchronises `stream`, then reads and clears this
+ * library's device status word for the current device.  Returns
+ * B300ATTN_ERR_TIMEOUT if any kernel gave up on a bounded wait since the last
+ * call (the kernel then stopped early and its outputs are not valid),
+ * B300ATTN_ERR_CUDA if the synchronisation failed, else B300ATTN_OK.
+ */
+int attn_device_status(cudaStream_t stream);
+
+/* Message describing the last non-OK status returned on this thread ("" if none). */
+const char* attn_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B300ATTN_H */

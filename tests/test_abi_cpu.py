@@ -1,0 +1,125 @@
+"""CPU tests of the C ABI: the library loads, exports every function the header
+declares, and rejects bad arguments on the host before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_transformer_attention_flashattention_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "b300attn.h")
+
+INVALID, UNSUPPORTED, WORKSPACE = -1, -2, -3
+FAKE = 0x10000  # a 16-byte aligned non-NULL value; validation fails before any use
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text,
+                                 flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def binding():
+    build.build()
+    from exact_transformer_attention_flashattention_b300 import binding as b
+    return b
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("attn_fwd", "attn_decode_splitkv", "lse_tree_combine"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(binding):
+    lib = ctypes.CDLL(binding.LIB_PATH)
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} declared in the header but not exported"
+        assert name in binding.SIGNATURES, f"{name} has no ctypes signature in the binding"
+
+
+def test_version(binding):
+    assert binding.lib().attn_version() >= 100
+
+
+def _fwd(lib, B=1, Hq=2, Hkv=2, N=16, d=64, causal=0, window=-1, scale=0.125, o_dtype=0,
+         ptr=FAKE, misalign=0):
+    p = ptr + misalign if ptr else None
+    return lib.attn_fwd(p, ptr, ptr, ptr, ptr, B, Hq, Hkv, N, d, causal, window, scale, None,
+                        o_dtype)
+
+
+def test_prefill_validation(binding):
+    lib = binding.lib()
+    assert _fwd(lib, B=-1) == INVALID
+    assert _fwd(lib, N=-5) == INVALID
+    assert _fwd(lib, Hq=3, Hkv=2) == INVALID
+    assert _fwd(lib, Hkv=0) == INVALID
+    assert _fwd(lib, d=96) == UNSUPPORTED
+    assert "d=96" in binding.last_error()
+    assert _fwd(lib, d=256) == UNSUPPORTED
+    assert _fwd(lib, ptr=0) == INVALID
+    assert _fwd(lib, misalign=8) == INVALID
+    assert _fwd(lib, causal=2) == INVALID
+    assert _fwd(lib, scale=float("nan")) == INVALID
+    assert _fwd(lib, scale=float("inf")) == INVALID
+    assert _fwd(lib, scale=-1.0) == INVALID
+    assert _fwd(lib, o_dtype=7) == INVALID
+
+
+def test_prefill_empty_is_a_noop(binding):
+    lib = binding.lib()
+    assert _fwd(lib, B=0, ptr=0) == 0
+    assert _fwd(lib, N=0, ptr=0) == 0
+    assert _fwd(lib, Hq=0, ptr=0) == 0
+
+
+def test_decode_chunk_and_workspace(binding):
+    assert binding.attn_decode_chunk(1 << 20, 2048) == 512
+    assert binding.attn_decode_chunk(8192, 16) == 512
+    assert binding.attn_decode_chunk(1000, 3) == 384  # ceil(1000/3)=334 -> multiple of 64
+    assert binding.attn_decode_chunk(1, 1) == 64
+    with pytest.raises(binding.B300AttnError):
+        binding.attn_decode_chunk(0, 4)
+    rows = 32 * 32 * 16
+    assert binding.attn_decode_workspace_size(32, 32, 16, 128) == 2 * rows * 4 + rows * 128 * 4
+    # 15 rows: m and l take 60 B each, padded to 256; o takes 15*64*4 = 3840 B
+    assert binding.attn_decode_workspace_size(1, 3, 5, 64) == 2 * 256 + 3840
+    assert binding.attn_decode_workspace_size(1, 1, 0, 64) == 0
+
+
+def _dec(lib, B=2, Hq=4, Hkv=2, L=100, d=128, S=4, ws=FAKE, ws_bytes=1 << 30, ptr=FAKE,
+         scale=0.1, o_dtype=0):
+    return lib.attn_decode_splitkv(ptr, ptr, ptr, ptr, ptr, ptr, B, Hq, Hkv, L, d, scale, S, ws,
+                                   ws_bytes, None, o_dtype)
+
+
+def test_decode_validation(binding):
+    lib = binding.lib()
+    assert _dec(lib, B=-1) == INVALID
+    assert _dec(lib, Hq=3) == INVALID
+    assert _dec(lib, d=80) == UNSUPPORTED
+    assert _dec(lib, S=0) == INVALID
+    assert _dec(lib, S=70000) == INVALID
+    assert _dec(lib, L=0) == INVALID
+    assert _dec(lib, ptr=0) == INVALID
+    assert _dec(lib, ws=0) == WORKSPACE
+    assert _dec(lib, ws_bytes=16) == WORKSPACE
+    assert "workspace" in binding.last_error()
+    assert _dec(lib, ws=FAKE + 16) == INVALID  # not 256-byte aligned
+    assert _dec(lib, scale=float("nan")) == INVALID
+    assert _dec(lib, B=0, ptr=0, ws=0) == 0
+
+
+def test_combine_validation(binding):
+    lib = binding.lib()
+    assert lib.lse_tree_combine(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 128, None, 0) == INVALID
+    assert lib.lse_tree_combine(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 128, None, 0) == INVALID
+    assert lib.lse_tree_combine(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, None, 0) == UNSUPPORTED
+    assert lib.lse_tree_combine(None, FAKE, FAKE, FAKE, FAKE, 4, 4, 64, None, 0) == INVALID
+    assert lib.lse_tree_combine(None, None, None, None, None, 0, 4, 64, None, 0) == 0
