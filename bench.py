@@ -135,19 +135,30 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.ok = False
+        self.index = device_index
         self.samples = []  # (time, sm_mhz, reasons)
         self.t0 = self.t1 = None
         self.max_mhz = None
+        self.error = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.h = None
+            try:  # NVML numbers all GPUs; find the one CUDA calls device_index
+                import torch
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(
+                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception as e:
+                self.error = "uuid lookup: " + repr(e)
+            if self.h is None:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.get_reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
             self.ok = True
-        except Exception as e:  # no NVML: clocks are reported as null
+        except Exception as e:  # no NVML: fall back to nvidia-smi
             self.error = repr(e)
 
     def _poll(self):
@@ -164,6 +175,21 @@ class ClockSampler:
             if mhz is not None:
                 self.samples.append((time.perf_counter(), mhz, rs))
             time.sleep(0.0005)
+
+    def _smi_fallback(self):
+        """One nvidia-smi query after the run when NVML gave no samples."""
+        import subprocess
+        try:
+            out = subprocess.run(
+                ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-i", str(self.index)],
+                capture_output=True, text=True, timeout=20).stdout.strip().splitlines()[0]
+            sm, mx, act = [x.strip() for x in out.split(",")]
+            return {"sm_mhz": float(sm), "sm_max_mhz": float(mx), "samples": 1,
+                    "in_timed_region": False, "reasons_bits": act, "source": "nvidia-smi after",
+                    "nvml_error": self.error}
+        except Exception as e:
+            return {"error": f"no clock samples (NVML: {self.error}; nvidia-smi: {e!r})"}
 
     def window(self, t0, t1):
         self.t0, self.t1 = t0, t1
@@ -182,7 +208,7 @@ class ClockSampler:
 
     def summary(self):
         if not self.ok or not self.samples:
-            return None
+            return self._smi_fallback()
         inside = [s for s in self.samples
                   if self.t0 is not None and self.t0 <= s[0] <= self.t1]
         use = inside or self.samples
@@ -276,7 +302,7 @@ def decode_case(w, dev):
     return q.to(dev), kc.to(dev), vc.to(dev), kv_len, kv_len.to(dev), ws, o, lse
 
 
-def bench_decode(w, steps, warmup, dist, peaks, peak_kind):
+def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
     from exact_transformer_attention_flashattention_b300 import binding as fa
     from exact_transformer_attention_flashattention_b300.inputs import decode_kv_bytes
     q, kc, vc, kv_len_host, kv_len, ws, o, lse = decode_case(w, "cuda")
@@ -293,7 +319,11 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind):
     def combine():
         fa.lse_tree_combine(m, l, po, out=o, lse=lse)
 
-    ms_full = time_launches(full, steps, warmup, dist)
+    if clocks is not None:
+        with clocks:
+            ms_full = time_launches(full, steps, warmup, dist, clocks)
+    else:
+        ms_full = time_launches(full, steps, warmup, dist)
     ms_part = time_launches(partials, steps, warmup, dist)
     ms_comb = time_launches(combine, steps, warmup, dist)
     assert fa.device_status() == 0, fa.last_error()
@@ -345,6 +375,36 @@ def e2e_prefill(w, steps, dist):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+def e2e_decode(w, steps, dist):
+    """Through the public API with host buffers.  The KV cache is state that a
+    decoder keeps resident in HBM, so it is copied once, outside the timed
+    region; every step copies q and kv_len from pinned host memory, runs the
+    decode and copies O and LSE back."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import decode_kv_bytes
+    q, kc, vc, kv_len_host, kv_len, ws, o, lse = decode_case(w, "cuda")
+    qh = q.cpu().pin_memory()
+    lh_in = kv_len_host.pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        q.copy_(qh, non_blocking=True)
+        kv_len.copy_(lh_in, non_blocking=True)
+        fa.attn_decode_splitkv(q, kc, vc, kv_len, w.num_splits, scale=w.scale, out=o, lse=lse,
+                               workspace=ws)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    ms = time_launches(step, steps, 2, dist)
+    gbs = decode_kv_bytes(kv_len_host, w.Hkv, w.d) * dist.world / (ms * 1e-3) / 1e9
+    return {"value": round(gbs, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": qh.numel() * 2 + lh_in.numel() * 4,
+            "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4, "ms_per_step": ms,
+            "note": "KV cache resident in HBM; q and kv_len copied in, O and LSE copied out"}
+
+
 # ----------------------------------------------------------------- CPU oracle
 def oracle_prefill_sample(w, rows_per_head: int, heads, inputs=None):
     """Time the float64 oracle on `heads` (b, h) pairs, `rows_per_head` query
@@ -393,9 +453,50 @@ def cpu_baseline(w, budget_s: float):
             "host_cores_available": len(os.sched_getaffinity(0))}
 
 
+def cpu_baseline_decode(w, budget_s: float):
+    """The oracle decode on whole (sequence, query head) rows until about
+    `budget_s` seconds of work; GB/s of K/V rows it read."""
+    import oracle
+    from exact_transformer_attention_flashattention_b300.inputs import decode_inputs
+    q, kc, vc, kv_len = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo,
+                                      w.kv_len_hi)
+    G = w.Hq // w.Hkv
+    secs = nbytes = 0.0
+    done = 0
+    for b in range(w.B):
+        for hk in range(w.Hkv):
+            heads = [(b, hk * G + g) for g in range(G)]
+            t0 = time.perf_counter()
+            oracle.decode(q, kc, vc, kv_len, scale=w.scale, heads=heads)
+            secs += time.perf_counter() - t0
+            nbytes += int(kv_len[b]) * w.d * 2 * 2
+            done += 1
+            if secs >= budget_s:
+                break
+        if secs >= budget_s:
+            break
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+            "cores": blas_threads() or len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{done} of {w.B * w.Hkv} (sequence, kv head) groups of {w.name}, every "
+                      f"query head of the group, float64 NumPy ({secs:.1f} s)",
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
 def run_reference(args, w, dist):
     """--impl reference: the oracle timed on bounded samples of the workload."""
     if dist.rank != 0:
+        return
+    if w.kind == "decode":
+        per = 150.0 / max(1, args.steps + args.warmup)
+        r = cpu_baseline_decode(w, per)
+        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": decode_config(w), "cpu_baseline": r,
+                "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
     inputs = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
@@ -435,6 +536,14 @@ def workload_config(w):
     return cfg
 
 
+def decode_config(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lmax": w.N, "d": w.d,
+            "num_splits": w.num_splits, "chunk": 512,
+            "kv_len": ("uniform [%d, %d]" % (w.kv_len_lo, w.kv_len_hi)) if w.kv_len_lo else "full",
+            "inputs": "bf16 i.i.d. N(0,1), seeded",
+            "l2": "inputs larger than L2 (K/V cache far above 126 MB); no flush"}
+
+
 def main():
     args = parse_args()
     from exact_transformer_attention_flashattention_b300.inputs import WORKLOADS
@@ -449,37 +558,53 @@ def main():
     torch.cuda.set_device(dist.local)
     from exact_transformer_attention_flashattention_b300 import binding  # noqa: F401 (loads .so)
     peaks, peak_kind = load_peaks()
-    if w.kind != "prefill":
-        raise SystemExit("the headline workload must be a prefill workload")
-
     clocks = ClockSampler(torch.cuda.current_device())
-    main_res = bench_prefill(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
-    value = main_res["flops"] * dist.world / (main_res["ms"] * 1e-3) / 1e12
+    if w.kind == "prefill":
+        main_res = bench_prefill(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
+        value = main_res["flops"] * dist.world / (main_res["ms"] * 1e-3) / 1e12
+        unit, ms, cfg, rf = "TFLOP/s", main_res["ms"], workload_config(w), main_res["roofline"]
+        launches = args.steps * main_res["launches_per_step"]
+    else:
+        main_res = bench_decode(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
+        value = main_res["kv_bytes"] * dist.world / (main_res["ms_per_call"] * 1e-3) / 1e9
+        unit, ms, cfg, rf = "GB/s", main_res["ms_per_call"], decode_config(w), main_res["roofline"]
+        launches = args.steps * main_res["launches_per_call"]
+        rf = dict(rf, note="dominant kernel of the step (the split partials); the step adds "
+                           "the tree combine")
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(main_res["ms"], 5),
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(w),
-        "roofline": main_res["roofline"], "gpu_launches": args.steps * main_res["launches_per_step"],
+        "data": "synthetic", "config": cfg, "roofline": rf, "gpu_launches": launches,
         "clocks": clocks.summary(),
     }
+    if w.kind == "decode":
+        line["kernels"] = main_res["kernels"]
     line["config"]["parallelism"] = f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
     if not args.no_e2e:
-        line["e2e"] = e2e_prefill(w, max(3, min(args.steps, 10)), dist)
+        e2e_steps = max(3, min(args.steps, 10))
+        line["e2e"] = e2e_prefill(w, e2e_steps, dist) if w.kind == "prefill" else \
+            e2e_decode(w, e2e_steps, dist)
     if not args.no_extra:
         extra = {}
         for name in ("decode_1m", "gqa_decode_batch32"):
+            if name == w.name:
+                continue
             extra[name] = bench_decode(WORKLOADS[name], max(3, min(args.steps, 50)),
                                        max(3, args.warmup), dist, peaks, peak_kind)
-        wn = WORKLOADS["window_encoder_8k"]
-        r = bench_prefill(wn, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks,
-                          peak_kind)
-        extra["window_encoder_8k"] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
-                                      "ms_per_call": r["ms"], "roofline": r["roofline"],
-                                      "config": workload_config(wn)}
+        for name in ("window_encoder_8k", "causal_prefill_4k"):
+            if name == w.name:
+                continue
+            wn = WORKLOADS[name]
+            r = bench_prefill(wn, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks,
+                              peak_kind)
+            extra[name] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
+                           "ms_per_call": r["ms"], "roofline": r["roofline"],
+                           "config": workload_config(wn)}
         line["extra"] = extra
     if dist.rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget) if w.kind == "prefill" else \
+            cpu_baseline_decode(w, args.cpu_budget)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
