@@ -28,6 +28,8 @@ SIGNATURES = {
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ,
                                  _P, _I]),
+    "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
+                                         _P, _I]),
     "attn_decode_partials": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "lse_tree_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I]),
     "attn_device_status": (_I, [_P]),
@@ -152,6 +154,34 @@ def attn_decode_splitkv(q, k_cache, v_cache, kv_len, num_splits: int, scale: flo
                                     _ptr(out), _ptr(lse), B, Hq, Hkv, Lmax, d, float(scale),
                                     int(num_splits), _ptr(workspace), workspace.numel(),
                                     _stream(stream), _odtype(out.dtype)))
+    return out, lse
+
+
+def attn_decode_splitkv_noalloc(q, k_cache, v_cache, kv_len, num_splits: int,
+                                scale: float | None = None, out=None, lse=None,
+                                out_dtype=torch.bfloat16, stream=None):
+    """Split-KV decode whose split partials live in the library's built-in
+    scratch (no workspace argument; the library allocates nothing).  For
+    callers that must not allocate device memory when they run decode.  Calls
+    share the scratch: do not let two of them overlap on the GPU."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(kv_len, "kv_len", torch.int32, 1)
+    B, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Lmax, Hkv, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(_lib.attn_decode_splitkv_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len),
+                                            _ptr(out), _ptr(lse), B, Hq, Hkv, Lmax, d,
+                                            float(scale), int(num_splits), _stream(stream),
+                                            _odtype(out.dtype)))
     return out, lse
 
 

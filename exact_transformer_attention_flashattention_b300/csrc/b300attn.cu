@@ -218,6 +218,44 @@ int launch_partials(int d, int GT, const void* k_cache, const void* v_cache,
   return d == 128 ? launch_decode_gt<128>(GT, k_cache, v_cache, p, stream)
                   : launch_decode_gt<64>(GT, k_cache, v_cache, p, stream);
 }
+// ---------------------------------------------------------------------------
+// Built-in scratch for attn_decode_splitkv_noalloc.  The split partials of
+// that entry point live in this file-scope device array instead of a
+// caller-supplied workspace.  Every device that loads this library holds the
+// array for the life of the process.  Calls share it, so calls that overlap on
+// the GPU race.  Nothing in it has to start at zero: the partial kernel writes
+// every (m, l, o) triple, including the empty ones, before the combine reads
+// it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;  // 40 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is looked up
+// with cudaGetSymbolAddress, once per device, on the first call made with that
+// device current, and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "device ordinal %d is out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+    if (!ptr) return fail(B300ATTN_ERR_CUDA, "cudaGetSymbolAddress returned NULL");
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return B300ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -305,6 +343,27 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   if ((rc = launch_partials(d, GT, k_cache, v_cache, p, stream)) != B300ATTN_OK) return rc;
   return launch_combine(p.part_m, p.part_l, p.part_o, o, lse, B * Hq, num_splits, d,
                         o_dtype == B300ATTN_F32, stream);
+}
+
+int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                const int* kv_len, void* o, float* lse, int B, int Hq, int Hkv,
+                                int max_kv_len, int d, float scale, int num_splits,
+                                cudaStream_t stream, int o_dtype) {
+  if (B < 0 || Hq < 0 || num_splits < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size");
+  if (B == 0 || Hq == 0) return B300ATTN_OK;
+  const size_t need = attn_decode_workspace_size(B, Hq, num_splits, d);
+  if (need > kNoAllocScratchBytes)
+    return fail(B300ATTN_ERR_WORKSPACE,
+                "attn_decode_splitkv_noalloc: B=%d Hq=%d num_splits=%d d=%d needs %zu bytes of "
+                "split partials, more than the built-in scratch of %zu bytes; use "
+                "attn_decode_splitkv with a workspace of your own",
+                B, Hq, num_splits, d, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != B300ATTN_OK) return rc;
+  return attn_decode_splitkv(q, k_cache, v_cache, kv_len, o, lse, B, Hq, Hkv, max_kv_len, d,
+                             scale, num_splits, scratch, kNoAllocScratchBytes, stream, o_dtype);
 }
 
 int lse_tree_combine(const float* part_m, const float* part_l, const float* part_o, void* o,

@@ -117,6 +117,40 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                         size_t workspace_bytes, cudaStream_t stream, int o_dtype);
 
 /*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv without a caller-supplied
+ * workspace, for callers that cannot allocate device memory at the point where
+ * they run decode.  Examples: a plugin whose host framework owns all device
+ * memory and forbids allocation inside its execution step, or a
+ * latency-critical loop where cudaMalloc, which may synchronise the whole
+ * device, is not acceptable.  Those callers still pass q, the caches, kv_len,
+ * o and lse; this entry point allocates nothing itself (no cudaMalloc, no
+ * cudaFree, no allocating library call).
+ *
+ * The split partials go to a scratch array compiled into the library (a
+ * file-scope __device__ array of 40 MiB = 41943040 bytes).  Every device that
+ * loads the library holds that array until the process exits.  A call whose
+ * partials would need more than that (attn_decode_workspace_size(B, Hq,
+ * num_splits, d) > 40 MiB) returns B300ATTN_ERR_WORKSPACE with a message; e.g.
+ * 1 sequence x 32 heads x 2048 splits x d=128 needs 33.5 MiB and fits.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents, so calls that overlap on the GPU (different
+ * streams, or host threads without ordering between them) race and corrupt
+ * each other's results: serialise them.  Nothing in the array needs clearing
+ * between calls, because each call rewrites every partial it later reads.
+ *
+ * The paper has no counterpart to this entry point; it exists for the
+ * allocation constraint above.  Arguments, layouts and errors are otherwise
+ * those of attn_decode_splitkv.
+ */
+int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                const int* kv_len, void* o, float* lse, int B, int Hq, int Hkv,
+                                int max_kv_len, int d, float scale, int num_splits,
+                                cudaStream_t stream, int o_dtype);
+
+/*
  * attn_decode_partials -- the first half of attn_decode_splitkv on its own:
  * writes the per-split partial triples (m, l, o) of every query head into
  * `workspace` (layout as described for attn_decode_splitkv) and does not merge
