@@ -93,14 +93,24 @@ def stored_traffic(kernel: str, workload: str):
 
 # ----------------------------------------------------------------- distributed
 class Dist:
-    def __init__(self, gpus: int):
+    """Rank bookkeeping for N independent replicas (one process per GPU, launched
+    by torchrun).  The only collectives are the barrier around the timed region
+    and the max of the per-rank times; the data path has none.  ``backend``
+    defaults to NCCL on a GPU machine and gloo elsewhere (the CPU tests)."""
+
+    def __init__(self, gpus: int, backend: str | None = None):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cpu"
         if self.world > 1:
+            import torch
             import torch.distributed as dist
-            dist.init_process_group("nccl")
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            self.device = "cuda" if backend == "nccl" else "cpu"
+            dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -111,7 +121,7 @@ class Dist:
         if not self.pg:
             return x
         import torch
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -243,6 +253,13 @@ def time_launches(fn, steps: int, warmup: int, dist: Dist, clocks=None):
         clocks.window(t0, t1)
     dist.barrier()
     return dist.max(start.elapsed_time(end) / steps)
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float, scale: float) -> float:
+    """Aggregate throughput of all ranks: every rank processes `units_per_rank`
+    units, the job takes the slowest rank's time `ms_max` (ms); `scale` converts
+    units/s to the reported unit (1e12 for TFLOP/s, 1e9 for GB/s)."""
+    return units_per_rank * world / (ms_max * 1e-3) / scale
 
 
 def roofline(achieved, peak, unit, bound, traffic, per_launch_units, unit_name):
@@ -561,12 +578,12 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device())
     if w.kind == "prefill":
         main_res = bench_prefill(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
-        value = main_res["flops"] * dist.world / (main_res["ms"] * 1e-3) / 1e12
+        value = whole_job_rate(main_res["flops"], dist.world, main_res["ms"], 1e12)
         unit, ms, cfg, rf = "TFLOP/s", main_res["ms"], workload_config(w), main_res["roofline"]
         launches = args.steps * main_res["launches_per_step"]
     else:
         main_res = bench_decode(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
-        value = main_res["kv_bytes"] * dist.world / (main_res["ms_per_call"] * 1e-3) / 1e9
+        value = whole_job_rate(main_res["kv_bytes"], dist.world, main_res["ms_per_call"], 1e9)
         unit, ms, cfg, rf = "GB/s", main_res["ms_per_call"], decode_config(w), main_res["roofline"]
         launches = args.steps * main_res["launches_per_call"]
         rf = dict(rf, note="dominant kernel of the step (the split partials); the step adds "
