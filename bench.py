@@ -131,6 +131,75 @@ class Dist:
 
 
 # ----------------------------------------------------------------- clocks
+class _Nvml:
+    """Read-only NVML access: the pynvml module when it is installed, else the
+    driver's libnvidia-ml.so.1 through ctypes.  Only clocks and clock-event
+    reasons are read; no setting of the GPU is changed."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str | None, index: int):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.kind = "pynvml"
+            self.nv = pynvml
+            h = None
+            if uuid:
+                try:
+                    h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+                except Exception:
+                    h = None
+            self.h = h if h is not None else pynvml.nvmlDeviceGetHandleByIndex(index)
+            self._reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            return
+        except ImportError:
+            pass
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.kind = "libnvidia-ml (ctypes)"
+        self.lib = lib
+        self.ct = ctypes
+        h = ctypes.c_void_p()
+        rc = -1
+        if uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+        if rc != 0:
+            raise RuntimeError(f"NVML handle lookup failed ({rc})")
+        self.h = h
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn if fn is not None else lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self) -> int:
+        if self.kind == "pynvml":
+            return self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+        v = self.ct.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        return int(v.value)
+
+    def max_sm_mhz(self) -> int:
+        if self.kind == "pynvml":
+            return self.nv.nvmlDeviceGetMaxClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+        v = self.ct.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+        return int(v.value)
+
+    def reasons(self) -> int:
+        if self.kind == "pynvml":
+            return int(self._reasons(self.h))
+        v = self.ct.c_ulonglong()
+        if self._reasons_fn(self.h, self.ct.byref(v)) != 0:
+            return 0
+        return int(v.value)
+
+
 class ClockSampler:
     """Polls SM clock and clock-event (throttle) reasons through NVML from a
     background thread; ``window`` marks the timed region and the summary uses
@@ -151,35 +220,27 @@ class ClockSampler:
         self.max_mhz = None
         self.error = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = None
+            uuid = None
             try:  # NVML numbers all GPUs; find the one CUDA calls device_index
                 import torch
-                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-                self.h = pynvml.nvmlDeviceGetHandleByUUID(
-                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+                u = str(torch.cuda.get_device_properties(device_index).uuid)
+                uuid = u if u.startswith("GPU-") else "GPU-" + u
             except Exception as e:
                 self.error = "uuid lookup: " + repr(e)
-            if self.h is None:
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.get_reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nvml = _Nvml(uuid, device_index)
+            self.max_mhz = self.nvml.max_sm_mhz()
             self.ok = True
-        except Exception as e:  # no NVML: fall back to nvidia-smi
+        except Exception as e:  # no NVML at all: one nvidia-smi query after the run
             self.error = repr(e)
 
     def _poll(self):
-        nv = self.nv
         while not self._stop.is_set():
             try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                mhz = self.nvml.sm_mhz()
             except Exception:
                 mhz = None
             try:
-                rs = self.get_reasons(self.h)
+                rs = self.nvml.reasons()
             except Exception:
                 rs = 0
             if mhz is not None:
@@ -228,7 +289,8 @@ class ClockSampler:
         names = [n for n, bit in self.REASONS.items() if bits & bit and n != "gpu_idle"]
         return {"sm_mhz": float(statistics.median(s[1] for s in use)),
                 "sm_max_mhz": self.max_mhz, "samples": len(use),
-                "in_timed_region": bool(inside), "reasons": names, "source": "NVML"}
+                "in_timed_region": bool(inside), "reasons": names,
+                "source": "NVML via " + self.nvml.kind}
 
 
 # ----------------------------------------------------------------- timing

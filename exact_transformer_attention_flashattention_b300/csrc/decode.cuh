@@ -43,7 +43,10 @@ struct DecodeParams {
 
 template <int D>
 struct DecCfg {
-  static constexpr int STAGES = (D == 128) ? 3 : 6;
+  // Two 64-key stages per CTA at d=128 (four at d=64) keep the ring at 64 KB,
+  // so that three CTAs share an SM and their streams overlap one another's
+  // start and end.
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
   static constexpr int HALF_BYTES = kDecSub * D * 2;  // K (or V) rows of one stage
   static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
   static constexpr int LPK = D / 8;          // lanes that share one key row (16 B each)
@@ -55,21 +58,34 @@ struct DecCfg {
 template <int D, int GT>
 struct DecSmem {
   static constexpr int RING = DecCfg<D>::STAGES * DecCfg<D>::STAGE_BYTES;
-  static constexpr int SCORES = kDecCWarps * 16 * GT * 4;            // per-warp s / p
-  static constexpr int MERGE_O = kDecCWarps * GT * D * 4;            // per-warp o
+  static constexpr int SCORES = kDecCWarps * 16 * GT * 4;            // per-warp scores
+  static constexpr int PROBS = kDecCWarps * 16 * GT * 8;             // per-warp (p, p) pairs
+  static constexpr int MERGE_O = kDecCWarps * GT * D * 4;            // per-warp o (aliases the ring)
   static constexpr int MERGE_ML = 2 * kDecCWarps * GT * 4;           // per-warp m, l
   static constexpr int BARS = 2 * DecCfg<D>::STAGES * 8;
+  static_assert(MERGE_O <= RING, "the merge buffer reuses the drained ring");
   static constexpr int OFF_SCORES = RING;
-  static constexpr int OFF_MO = OFF_SCORES + SCORES;
-  static constexpr int OFF_ML = OFF_MO + MERGE_O;
+  static constexpr int OFF_PROBS = OFF_SCORES + SCORES;
+  static constexpr int OFF_ML = OFF_PROBS + PROBS;
   static constexpr int OFF_BARS = (OFF_ML + MERGE_ML + 15) & ~15;
   static constexpr int BYTES = OFF_BARS + BARS + 128;  // + alignment slack
 };
 
+// Eight bf16 (one 16-byte load) as four f32 pairs.
+__device__ __forceinline__ void unpack8(const uint4 w, float2 (&f)[4]) {
+  f[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+  f[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+  f[2] = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
+  f[3] = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
+}
+
 // One CTA: (split = blockIdx.x, kv head x head group = blockIdx.y, sequence = blockIdx.z).
 // GT query heads per CTA (the whole GQA group when it is 1, 2, 4 or 8 heads).
+// Arithmetic on f32 pairs (fma.rn.f32x2) halves the instruction count of the
+// dot products and of the P V accumulation, which keeps the kernel on the
+// memory roofline instead of the issue rate.
 template <int D, int GT>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using C = DecCfg<D>;
@@ -82,7 +98,8 @@ __global__ void __launch_bounds__(kDecThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
   float* s_sm = reinterpret_cast<float*>(smem + L::OFF_SCORES);
-  float* mo_sm = reinterpret_cast<float*>(smem + L::OFF_MO);
+  float2* p_sm = reinterpret_cast<float2*>(smem + L::OFF_PROBS);
+  float* mo_sm = reinterpret_cast<float*>(smem);  // after the last stage is consumed
   float* mm_sm = reinterpret_cast<float*>(smem + L::OFF_ML);
   float* ml_sm = mm_sm + kDecCWarps * GT;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
@@ -138,24 +155,23 @@ __global__ void __launch_bounds__(kDecThreads)
   const int grp = lane / LPK;  // key group within the warp
   const int li = lane % LPK;   // 8 consecutive elements of d: [8*li, 8*li+8)
   float* s_w = s_sm + warp * 16 * GT;
+  float2* p_w = p_sm + warp * 16 * GT;
 
-  float qf[GT][8];  // q * scale * log2(e), this lane's slice of d
+  float2 qf[GT][4];  // q * scale * log2(e), this lane's slice of d, as pairs
 #pragma unroll
   for (int g = 0; g < GT; ++g) {
     const uint4 w = *reinterpret_cast<const uint4*>(
         p.q + (static_cast<size_t>(b) * p.Hq + hq0 + g) * D + 8 * li);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    unpack8(w, qf[g]);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qf[g][2 * e] = bf16lo_to_f32(u[e]) * p.scale_log2;
-      qf[g][2 * e + 1] = bf16hi_to_f32(u[e]) * p.scale_log2;
-    }
+    for (int e = 0; e < 4; ++e)
+      qf[g][e] = make_float2(qf[g][e].x * p.scale_log2, qf[g][e].y * p.scale_log2);
   }
-  float acc[GT][8];
+  float2 acc[GT][4];
 #pragma unroll
   for (int g = 0; g < GT; ++g)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
   float m_ref[GT];  // base-2 running maximum per head (warp-uniform)
 #pragma unroll
   for (int g = 0; g < GT; ++g) m_ref[g] = -INFINITY;
@@ -175,20 +191,15 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
     for (int kk = 0; kk < KPG; ++kk) {
       const int key = wkey0 + grp * KPG + kk;
-      const uint4 w = *reinterpret_cast<const uint4*>(Ks + key * (D * 2) + li * 16);
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-      float kf[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16lo_to_f32(u[e]);
-        kf[2 * e + 1] = bf16hi_to_f32(u[e]);
-      }
+      float2 kf[4];
+      unpack8(*reinterpret_cast<const uint4*>(Ks + key * (D * 2) + li * 16), kf);
 #pragma unroll
       for (int g = 0; g < GT; ++g) {
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
-        val[kk * GT + g] = a;
+        float2 a = fmul2(qf[g][0], kf[0]);
+        a = ffma2(qf[g][1], kf[1], a);
+        a = ffma2(qf[g][2], kf[2], a);
+        a = ffma2(qf[g][3], kf[3], a);
+        val[kk * GT + g] = a.x + a.y;
       }
     }
     // ---- butterfly reduce-scatter over the LPK lanes of the group
@@ -242,8 +253,9 @@ __global__ void __launch_bounds__(kDecThreads)
       if (mn > m_ref[g] + kRescaleThreshold) {  // warp-uniform
         const float alpha = ex2_approx(m_ref[g] - mn);
         m_ref[g] = mn;
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        for (int e = 0; e < 4; ++e) acc[g][e] = fmul2(acc[g][e], a2);
         if (myg == g) lsum *= alpha;
       }
       if (myg == g) mu_mine = (m_ref[g] == -INFINITY) ? 0.f : m_ref[g];
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(kDecThreads)
       const int v = lane + 32 * t;
       const float pv = ex2_approx(x[t] - mu_mine);
       lsum += pv;
-      if (v < 16 * GT) s_w[v] = pv;
+      if (v < 16 * GT) p_w[v] = make_float2(pv, pv);
     }
     __syncwarp();
 
@@ -262,19 +274,13 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int kk = 0; kk < KPG; ++kk) {
       const int kl = grp * KPG + kk;
       if (wkey0 + kl < nvalid) {
-        const uint4 w = *reinterpret_cast<const uint4*>(Vs + (wkey0 + kl) * (D * 2) + li * 16);
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-        float vf[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          vf[2 * e] = bf16lo_to_f32(u[e]);
-          vf[2 * e + 1] = bf16hi_to_f32(u[e]);
-        }
+        float2 vf[4];
+        unpack8(*reinterpret_cast<const uint4*>(Vs + (wkey0 + kl) * (D * 2) + li * 16), vf);
 #pragma unroll
         for (int g = 0; g < GT; ++g) {
-          const float pg = s_w[kl * GT + g];
+          const float2 pg = p_w[kl * GT + g];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pg, vf[e], acc[g][e]);
+          for (int e = 0; e < 4; ++e) acc[g][e] = ffma2(vf[e], pg, acc[g][e]);
         }
       }
     }
@@ -282,21 +288,27 @@ __global__ void __launch_bounds__(kDecThreads)
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
 
-  // ---- merge the key groups of the warp, then the four warps
+  // ---- merge the key groups of the warp, then the four warps.  The merge
+  // buffer for o reuses the ring: every stage has landed and been consumed.
 #pragma unroll
   for (int mask = LPK; mask < 32; mask <<= 1) {
 #pragma unroll
     for (int g = 0; g < GT; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], mask);
+      for (int e = 0; e < 4; ++e) {
+        acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, mask);
+        acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, mask);
+      }
   }
 #pragma unroll
   for (int mask = GT; mask < 32; mask <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, mask);
+  named_bar_sync(1, kDecCWarps * 32);  // every warp is done reading the ring
   if (lane < LPK) {
 #pragma unroll
     for (int g = 0; g < GT; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mo_sm[(warp * GT + g) * D + 8 * lane + e] = acc[g][e];
+      for (int e = 0; e < 4; ++e)
+        *reinterpret_cast<float2*>(&mo_sm[(warp * GT + g) * D + 8 * lane + 2 * e]) = acc[g][e];
   }
 #pragma unroll
   for (int g = 0; g < GT; ++g)
