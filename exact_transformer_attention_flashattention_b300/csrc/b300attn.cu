@@ -3,6 +3,7 @@
 // their status words can be read back by attn_device_status.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -77,6 +78,26 @@ int set_smem(K kernel, int bytes) {
   return B300ATTN_OK;
 }
 
+// Number of SMs of the current device (cached per device).
+int sm_count(int* out) {
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev >= 0 && dev < kMaxDev && cache[dev] > 0) {
+    *out = cache[dev];
+    return B300ATTN_OK;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+  if (n < 1) return fail(B300ATTN_ERR_CUDA, "device reports %d SMs", n);
+  if (dev >= 0 && dev < kMaxDev) cache[dev] = n;
+  *out = n;
+  return B300ATTN_OK;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 template <int D>
@@ -95,9 +116,11 @@ int launch_prefill(const void* q, const void* k, const void* v, const PrefillPar
                         CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
     return rc;
   if ((rc = set_smem(prefill_kernel<D>, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
-  const long long grid = static_cast<long long>(p.nqb) * p.Hq * p.B;
-  prefill_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk,
-                                                                                       tv, p);
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != B300ATTN_OK) return rc;
+  // persistent: one CTA per SM (the kernel's shared memory admits no second one)
+  const int grid = std::min(p.n_items, sms);
+  prefill_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return B300ATTN_OK;
@@ -295,8 +318,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.nqb = (N + 255) / 256;
   // a zero scale is kept strictly positive so that masked (-inf) scores stay -inf
   p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
-  const long long grid = static_cast<long long>(p.nqb) * Hq * B;
-  if (grid > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "grid too large");
+  const long long items = static_cast<long long>(p.nqb) * Hq * B;
+  if (items > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
+  p.n_items = static_cast<int>(items);
   return d == 128 ? launch_prefill<128>(q, k, v, p, stream) : launch_prefill<64>(q, k, v, p, stream);
 }
 

@@ -10,8 +10,14 @@
 // Key tiles that a row block cannot see (causal future, outside the local
 // window of the Arabic context-length thread, point 1) are skipped.
 //
-// CTA layout (384 threads, one CTA per SM):
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a STAGES-deep ring
+// Persistent CTAs, one per SM: each CTA walks a list of work items (a 256-row
+// query block of one (batch, head)), so that the loads and MMAs of the next
+// item overlap the epilogue of the current one.  Items are dealt to the CTAs
+// in a zig-zag over a heaviest-first order (causal), which balances the
+// triangular work without any global counter.
+//
+// CTA layout (384 threads):
+//   warp 0      TMA producer: Q tiles of each item, then K_j, V_j into a STAGES-deep ring
 //   warp 1      MMA issuer (lane 0): S_i = Q_i K_j^T, O_i += P_i V_j
 //   warp 2      tensor-memory allocator
 //   warp 3      idle
@@ -23,6 +29,13 @@
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_0 cols [0,128)   S_1 cols [128,256)   O_0 [256,256+D)   O_1 [256+D,256+2D)
 //   P_i (bf16 pairs) overwrites cols [0,64) of S_i once S_i is in registers.
+//
+// Barriers (all waits bounded in time):
+//   q_full[i] / q_empty[i]   Q tile i of an item landed / its last S MMA done
+//   kv_full[s] / kv_empty[s] ring stage s landed / its MMAs done
+//   s_full[i]                S_i of the current key tile is in tensor memory
+//   p_full[i]                P_i written (and O_i rescaled) by the 128 softmax threads
+//   o_full[i] / o_empty[i]   O_i of an item complete / read out by the epilogue
 #pragma once
 
 #include "ptx.cuh"
@@ -39,6 +52,7 @@ struct PrefillParams {
   int B, Hq, Hkv, N;
   int causal, window, o_f32;
   int nqb;           // number of 256-row query blocks
+  int n_items;       // nqb * B * Hq
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -57,6 +71,50 @@ struct PrefillCfg {
   static_assert(BM == BN, "Q and K/V tiles share one byte layout");
 };
 
+// The k-th work item of CTA c among G CTAs: zig-zag over the item order.
+__device__ __forceinline__ int prefill_item(int c, int k, int G) {
+  return (k & 1) ? k * G + (G - 1 - c) : k * G + c;
+}
+
+// What one work item covers: query block qb of (b, h), and the key-tile
+// range [jlo[i], jhi[i]] of each of its two Q tiles.
+struct PrefillItem {
+  int qb, b, h, hk;
+  int jlo[2], jhi[2];
+  bool act[2];
+  int J0, J1;
+};
+
+__device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p, int item) {
+  constexpr int BN = 128;
+  PrefillItem it;
+  const int BH = p.B * p.Hq;
+  int bh;
+  if (p.causal) {  // heaviest query blocks first
+    it.qb = p.nqb - 1 - item / BH;
+    bh = item % BH;
+  } else {  // all blocks of one head together: they share its K/V in L2
+    it.qb = item % p.nqb;
+    bh = item / p.nqb;
+  }
+  it.b = bh / p.Hq;
+  it.h = bh % p.Hq;
+  it.hk = it.h / (p.Hq / p.Hkv);
+  const int N = p.N;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = it.qb * 256 + i * 128;
+    it.act[i] = r0 < N;
+    const int r1 = min(r0 + 127, N - 1);
+    const int klo = (p.window >= 0) ? max(0, r0 - p.window) : 0;
+    const int khi = p.causal ? r1 : ((p.window >= 0) ? min(N - 1, r1 + p.window) : N - 1);
+    it.jlo[i] = klo / BN;
+    it.jhi[i] = khi / BN;
+  }
+  it.J0 = it.act[1] ? min(it.jlo[0], it.jlo[1]) : it.jlo[0];
+  it.J1 = it.act[1] ? max(it.jhi[0], it.jhi[1]) : it.jhi[0];
+  return it;
+}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -71,54 +129,35 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::RING_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;  // [2]
-  uint64_t* p_full = s_full + 2;         // [2]
-  uint64_t* o_full = p_full + 2;         // [2]
-  uint64_t* mma_done = o_full + 2;
+  uint64_t* q_full = bars;                // [2]
+  uint64_t* q_empty = q_full + 2;         // [2]
+  uint64_t* kv_full = q_empty + 2;        // [STAGES]
+  uint64_t* kv_empty = kv_full + STAGES;  // [STAGES]
+  uint64_t* s_full = kv_empty + STAGES;   // [2]
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* o_full = p_full + 2;          // [2]
+  uint64_t* o_empty = o_full + 2;         // [2]
+  uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- which (query block, head, batch) this CTA owns; causal: heaviest first
-  const int BH = p.B * p.Hq;
-  int qb = blockIdx.x / BH;
-  if (p.causal) qb = p.nqb - 1 - qb;
-  const int bh = blockIdx.x % BH;
-  const int b = bh / p.Hq;
-  const int h = bh % p.Hq;
-  const int hk = h / (p.Hq / p.Hkv);
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
   const int N = p.N;
 
-  // ---- key-tile range [jlo, jhi] of each Q tile
-  int jlo[2], jhi[2];
-  bool act[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r0 = qb * 256 + i * 128;
-    act[i] = r0 < N;
-    const int r1 = min(r0 + 127, N - 1);
-    const int klo = (p.window >= 0) ? max(0, r0 - p.window) : 0;
-    const int khi = p.causal ? r1 : ((p.window >= 0) ? min(N - 1, r1 + p.window) : N - 1);
-    jlo[i] = klo / BN;
-    jhi[i] = khi / BN;
-  }
-  const int J0 = act[1] ? min(jlo[0], jlo[1]) : jlo[0];
-  const int J1 = act[1] ? max(jhi[0], jhi[1]) : jhi[0];
-
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 128);
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -137,165 +176,215 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup
+  // 0 (producer, MMA, allocator, idle) gives back to 64 and the two softmax
+  // warpgroups take 216: 128 x 64 + 256 x 216 = 63488 <= 64512.
+  if (warp < 4) {
+  setmaxnreg_dec<120>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
-      for (int i = 0; i < 2; ++i)
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_4d(sQ + i * C::TILE_BYTES + c * (C::BM * 128), &tm_q, q_full, c * 64, h,
-                      qb * 256 + i * 128, b);
-      const int nloads = 2 * (J1 - J0 + 1);  // K_j, V_j alternate in the ring
-      int issued = 0;
-      for (; issued < nloads; ++issued) {
-        const int s = issued % STAGES;
-        if (issued >= STAGES &&
-            !mbar_wait(&kv_empty[s], ((issued / STAGES) - 1) & 1, &g_prefill_status,
-                       kStatusProducer))
-          break;
-        mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
-        const int j = J0 + issued / 2;
-        const CUtensorMap* tm = (issued & 1) ? &tm_v : &tm_k;
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_4d(sRing + s * C::TILE_BYTES + c * (BN * 128), tm, &kv_full[s], c * 64, hk,
-                      j * BN, b);
+      bool ok = true;
+      int issued = 0;  // K/V ring loads issued so far (all items)
+      int k = 0;       // items of this CTA started
+      for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+           item = prefill_item(c, ++k, G)) {
+        const PrefillItem it = prefill_item_info(p, item);
+        // Q tile i of this item, once the last S MMA of the previous item
+        // has read the buffer.
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (k > 0 && !(ok = mbar_wait(&q_empty[i], (k - 1) & 1, &g_prefill_status,
+                                        kStatusProducer)))
+            break;
+          mbar_arrive_expect_tx(&q_full[i], C::TILE_BYTES);
+          for (int cc = 0; cc < C::DCH; ++cc)
+            tma_load_4d(sQ + i * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, &q_full[i], cc * 64,
+                        it.h, it.qb * 256 + i * 128, it.b);
+        }
+        const int nloads = 2 * (it.J1 - it.J0 + 1);  // K_j, V_j alternate in the ring
+        for (int u = 0; u < nloads && ok; ++u, ++issued) {
+          const int s = issued % STAGES;
+          if (issued >= STAGES &&
+              !(ok = mbar_wait(&kv_empty[s], ((issued / STAGES) - 1) & 1, &g_prefill_status,
+                               kStatusProducer)))
+            break;
+          mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
+          const int j = it.J0 + u / 2;
+          const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
+          for (int cc = 0; cc < C::DCH; ++cc)
+            tma_load_4d(sRing + s * C::TILE_BYTES + cc * (BN * 128), tm, &kv_full[s], cc * 64,
+                        it.hk, j * BN, it.b);
+        }
       }
       // Every issued copy has landed before the CTA may exit (a no-op wait on
       // the normal path, where the MMA warp already consumed them all).
       for (int u = max(0, issued - STAGES); u < issued; ++u)
         mbar_wait(&kv_full[u % STAGES], (u / STAGES) & 1, &g_prefill_status, kStatusProducer);
-      mbar_wait(q_full, 0, &g_prefill_status, kStatusProducer);
+      if (k > 0)
+        for (int i = 0; i < 2; ++i)
+          mbar_wait(&q_full[i], (k - 1) & 1, &g_prefill_status, kStatusProducer);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(128, BN, false);
-      const uint32_t idO = idesc_bf16_f32(128, D, true);
-      const uint32_t sq = smem_u32(sQ);
-      const uint32_t sr = smem_u32(sRing);
-      uint32_t pcnt[2] = {0u, 0u};
+    // The whole warp runs this loop (waits included); one elected lane issues
+    // each tcgen05 instruction.  Descriptors are a base plus constant offsets.
+    const uint32_t idS = idesc_bf16_f32(128, BN, false);
+    const uint32_t idO = idesc_bf16_f32(128, D, true);
+    const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(sRing), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(sRing), BN * 128, 1024);
+    uint32_t pcnt[2] = {0u, 0u};  // p_full phases consumed, per Q tile
+    uint32_t ocnt[2] = {0u, 0u};  // items in which Q tile i was active
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_prefill_status, kStatusMma));
+    };
 
-      // S_i = Q_i K^T: K-major operands, 16 elements of d per instruction.
-      auto issue_S = [&](int i, int stage) {
+    // S_i = Q_i K^T: K-major operands, 16 elements of d per instruction.
+    auto issue_S = [&](int i, int stage) {
+      const uint64_t a0 = dq0 + static_cast<uint64_t>((i * C::TILE_BYTES) >> 4);
+      const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (C::BM * 128) + (k & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sq + i * C::TILE_BYTES + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sr + stage * C::TILE_BYTES + off, 16, 1024);
-          umma_ss(tmem + i * 128, a, bd, idS, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[i]);
-      };
-      // O_i += P_i V: P (bf16 pairs) from tensor memory, V MN-major in shared
-      // memory, 16 keys per instruction.
-      auto issue_PV = [&](int i, int stage, bool accumulate) {
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t bd = smem_desc_sw128(sr + stage * C::TILE_BYTES + k * 16 * 128,
-                                              BN * 128, 1024);
-          umma_ts(tmem + 256 + i * D, tmem + i * 128 + k * 8, bd, idO,
-                  (accumulate || k > 0) ? 1u : 0u);
-        }
-      };
-
-      bool ok = mbar_wait(q_full, 0, &g_prefill_status, kStatusMma);
-      if (ok) ok = mbar_wait(&kv_full[0], 0, &g_prefill_status, kStatusMma);
-      if (ok) {
-        tc_fence_after();
-        for (int i = 0; i < 2; ++i)
-          if (act[i] && J0 >= jlo[i] && J0 <= jhi[i]) issue_S(i, 0);
-        umma_commit(&kv_empty[0]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4;
+        umma_ss_warp(tmem + i * 128, a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
       }
-      int t = 1;  // ring position of V_j
-      for (int j = J0; j <= J1 && ok; ++j, t += 2) {
+      umma_commit_warp(&s_full[i]);
+    };
+    // O_i += P_i V: P (bf16 pairs) from tensor memory, V MN-major in shared
+    // memory, 16 keys per instruction.
+    auto issue_PV = [&](int i, int stage, bool accumulate) {
+      const uint64_t b0 = dv0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        umma_ts_warp(tmem + 256 + i * D, tmem + i * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4), idO,
+                     (accumulate || kk > 0) ? 1u : 0u);
+    };
+
+    bool ok = true;
+    int t0 = 0;  // ring position of this item's first load (K_J0)
+    int k = 0;
+    for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+         item = prefill_item(c, ++k, G)) {
+      const PrefillItem it = prefill_item_info(p, item);
+      for (int i = 0; i < 2 && ok; ++i) ok = wait(&q_full[i], k & 1);
+      if (ok) ok = wait(&kv_full[t0 % STAGES], (t0 / STAGES) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      for (int i = 0; i < 2; ++i) {
+        if (it.act[i] && it.J0 >= it.jlo[i] && it.J0 <= it.jhi[i]) {
+          issue_S(i, t0 % STAGES);
+          if (it.jhi[i] == it.J0) umma_commit_warp(&q_empty[i]);
+        } else if (!it.act[i]) {
+          umma_commit_warp(&q_empty[i]);  // no S MMA reads this Q tile
+        }
+      }
+      umma_commit_warp(&kv_empty[t0 % STAGES]);
+      int t = t0 + 1;  // ring position of V_j
+      for (int j = it.J0; j <= it.J1 && ok; ++j, t += 2) {
         const int sv = t % STAGES;
-        if (!(ok = mbar_wait(&kv_full[sv], (t / STAGES) & 1, &g_prefill_status, kStatusMma)))
-          break;
+        if (!(ok = wait(&kv_full[sv], (t / STAGES) & 1))) break;
         tc_fence_after();
-        const bool has_next = j < J1;
+        const bool has_next = j < it.J1;
         const int sk = (t + 1) % STAGES;
         bool k_ready = false;
         for (int i = 0; i < 2 && ok; ++i) {
-          if (act[i] && j >= jlo[i] && j <= jhi[i]) {
-            if (!(ok = mbar_wait(&p_full[i], pcnt[i] & 1, &g_prefill_status, kStatusMma))) break;
+          if (it.act[i] && j >= it.jlo[i] && j <= it.jhi[i]) {
+            if (!(ok = wait(&p_full[i], pcnt[i] & 1))) break;
             ++pcnt[i];
+            if (j == it.jlo[i] && ocnt[i] > 0 && !(ok = wait(&o_empty[i], (ocnt[i] - 1) & 1)))
+              break;
             tc_fence_after();
-            issue_PV(i, sv, j != jlo[i]);
-            if (j == jhi[i]) umma_commit(&o_full[i]);
+            issue_PV(i, sv, j != it.jlo[i]);
+            if (j == it.jhi[i]) {
+              umma_commit_warp(&o_full[i]);
+              ++ocnt[i];
+            }
           }
-          if (has_next && act[i] && j + 1 >= jlo[i] && j + 1 <= jhi[i]) {
+          if (has_next && it.act[i] && j + 1 >= it.jlo[i] && j + 1 <= it.jhi[i]) {
             if (!k_ready) {
-              if (!(ok = mbar_wait(&kv_full[sk], ((t + 1) / STAGES) & 1, &g_prefill_status,
-                                   kStatusMma)))
-                break;
+              if (!(ok = wait(&kv_full[sk], ((t + 1) / STAGES) & 1))) break;
               tc_fence_after();
               k_ready = true;
             }
             issue_S(i, sk);
+            if (j + 1 == it.jhi[i]) umma_commit_warp(&q_empty[i]);
           }
         }
         if (!ok) break;
-        umma_commit(&kv_empty[sv]);
+        umma_commit_warp(&kv_empty[sv]);
         if (has_next) {
-          if (!k_ready &&
-              !(ok = mbar_wait(&kv_full[sk], ((t + 1) / STAGES) & 1, &g_prefill_status,
-                               kStatusMma)))
-            break;
-          umma_commit(&kv_empty[sk]);
+          if (!k_ready && !(ok = wait(&kv_full[sk], ((t + 1) / STAGES) & 1))) break;
+          umma_commit_warp(&kv_empty[sk]);
         }
       }
-      // All MMAs of this CTA complete before tensor memory is released.
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0, &g_prefill_status, kStatusMma);
+      t0 += 2 * (it.J1 - it.J0 + 1);
     }
-  } else if (warp >= 4) {
+    // All MMAs of this CTA complete before tensor memory is released.
+    umma_commit_warp(mma_done);
+    wait(mma_done, 0);
+  }
+  } else {
+    setmaxnreg_inc<192>();
     // ================================================================ softmax
     const int i = (warp - 4) >> 2;   // Q tile of this warpgroup
     const int quarter = warp & 3;    // tensor-memory lane quarter this warp may access
     const int r = quarter * 32 + lane;
-    const int r0 = qb * 256 + i * 128;
-    const int row = r0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + i * 128;
     const uint32_t tO = tmem + lane_off + 256 + i * D;
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const int window = p.window;
-    float m_ref = -INFINITY;  // base-2 running maximum actually used for P
-    float l = 0.f;
     bool ok = true;
-    if (act[i]) {
-      int n = 0;
-      for (int j = jlo[i]; j <= jhi[i]; ++j, ++n) {
-        ok = mbar_wait(&s_full[i], n & 1, &g_prefill_status, kStatusSoftmax);
+    uint32_t scnt = 0;  // s_full phases consumed
+    uint32_t ocnt = 0;  // items in which this Q tile was active
+    int k = 0;
+    for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+         item = prefill_item(c, ++k, G)) {
+      const PrefillItem it = prefill_item_info(p, item);
+      if (!it.act[i]) continue;
+      const int r0 = it.qb * 256 + i * 128;
+      const int row = r0 + r;
+      float m_ref = -INFINITY;  // base-2 running maximum actually used for P
+      float l = 0.f;
+      for (int j = it.jlo[i]; j <= it.jhi[i]; ++j, ++scnt) {
+        ok = mbar_wait(&s_full[i], scnt & 1, &g_prefill_status, kStatusSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // S row of this thread: four 32-column loads in flight, one wait
+        uint32_t u[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, u[cc]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) reg_fence(u[cc]);
         float s[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32_wait(tS + c * 32, u);
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[e]);
-        }
+          for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(u[cc][e]);
         const int kv0 = j * BN;
         const bool need_mask =
             (kv0 + BN > N) || (causal && kv0 + BN - 1 > r0) ||
             (window >= 0 && (r0 + 127 - kv0 > window || (!causal && kv0 + BN - 1 - r0 > window)));
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int key = kv0 + c;
+          for (int cc = 0; cc < 128; ++cc) {
+            const int key = kv0 + cc;
             bool vis = key < N;
             if (causal) vis = vis && key <= row;
             if (window >= 0) vis = vis && (row - key <= window) && (causal || key - row <= window);
-            if (!vis) s[c] = -INFINITY;
+            if (!vis) s[cc] = -INFINITY;
           }
         }
-        float mx = s[0];
+        // row maximum: four independent chains of three-input max
+        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int cc = 0; cc < 128; cc += 8)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
+        const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
         const float m_new = fmaxf(m_ref, mx * sl2);
         const bool resc = m_new > m_ref + kRescaleThreshold;
         float alpha = 1.f;
@@ -305,80 +394,95 @@ __global__ void __launch_bounds__(384, 1)
           l *= alpha;
         }
         const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        // P = 2^(s*scale*log2e - m), row sum in f32, bf16 pairs into tensor memory
+        // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
+        // in four packed partial sums, bf16 pairs into tensor memory
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 nmu2 = make_float2(neg_mu, neg_mu);
+        float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * e], sl2, neg_mu));
-            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * e + 1], sl2, neg_mu));
-            l += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            const float2 x =
+                ffma2(make_float2(s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1]), sl2x2, nmu2);
+            const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            lacc[e & 3] = fadd2(lacc[e & 3], pe);
+            pk[e] = pack_bf16x2(pe.x, pe.y);
           }
-          tmem_st16(tS + c * 16, pk);
+          tmem_st16(tS + cc * 16, pk);
+        }
+        {
+          const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
+          const float2 t = fadd2(a, b2);
+          l += t.x + t.y;
         }
         // Rescale this row of O (only rows whose maximum moved; the previous
         // P V of this tile is complete because S_i(j) was committed after it).
-        if (n > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > it.jlo[i] && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32_wait(tO + c * 32, u);
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t w[32];
+            tmem_ld32_wait(tO + cc * 32, w);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(tO + c * 32, u);
+            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+            tmem_st32(tO + cc * 32, w);
           }
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[i]);
       }
+      if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (ok) {
-        ok = mbar_wait(&o_full[i], 0, &g_prefill_status, kStatusSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        const bool store = row < N;
-        const size_t orow = (static_cast<size_t>(b) * N + row) * p.Hq + h;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32_wait(tO + c * 32, u);
-          if (store) {
-            if (p.o_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
+      ok = mbar_wait(&o_full[i], ocnt & 1, &g_prefill_status, kStatusSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ++ocnt;
+      tc_fence_after();
+      uint32_t u[D / 32][32];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                dst[e] = make_float4(__uint_as_float(u[4 * e]) * inv_l,
-                                     __uint_as_float(u[4 * e + 1]) * inv_l,
-                                     __uint_as_float(u[4 * e + 2]) * inv_l,
-                                     __uint_as_float(u[4 * e + 3]) * inv_l);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D +
-                                                    c * 32);
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, u[cc]);
+      tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * inv_l,
-                                  __uint_as_float(u[8 * e + 1]) * inv_l);
-                w.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * inv_l,
-                                  __uint_as_float(u[8 * e + 3]) * inv_l);
-                w.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * inv_l,
-                                  __uint_as_float(u[8 * e + 5]) * inv_l);
-                w.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * inv_l,
-                                  __uint_as_float(u[8 * e + 7]) * inv_l);
-                dst[e] = w;
-              }
+      for (int cc = 0; cc < D / 32; ++cc) reg_fence(u[cc]);
+      // O_i is in registers: the next item's first P V may overwrite it.
+      tc_fence_before();
+      mbar_arrive(&o_empty[i]);
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if (row < N) {
+        const size_t orow = (static_cast<size_t>(it.b) * N + row) * p.Hq + it.h;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          if (p.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(u[cc][4 * e]) * inv_l,
+                                   __uint_as_float(u[cc][4 * e + 1]) * inv_l,
+                                   __uint_as_float(u[cc][4 * e + 2]) * inv_l,
+                                   __uint_as_float(u[cc][4 * e + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D +
+                                                  cc * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(u[cc][8 * e + 0]) * inv_l,
+                                __uint_as_float(u[cc][8 * e + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(u[cc][8 * e + 2]) * inv_l,
+                                __uint_as_float(u[cc][8 * e + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(u[cc][8 * e + 4]) * inv_l,
+                                __uint_as_float(u[cc][8 * e + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(u[cc][8 * e + 6]) * inv_l,
+                                __uint_as_float(u[cc][8 * e + 7]) * inv_l);
+              dst[e] = w;
             }
           }
         }
-        if (store)
-          p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] =
-              (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * N + row] =
+            (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
   }
