@@ -31,12 +31,14 @@
 //   P_i (bf16 pairs) overwrites cols [0,64) of S_i once S_i is in registers.
 //
 // Barriers (all waits bounded in time):
-//   q_full[i] / q_empty[i]   Q tile i of an item landed / its last S MMA done
+//   q_full / q_empty         Q tile i of an item landed / its last S MMA done (per Q buffer)
 //   kv_full[s] / kv_empty[s] ring stage s landed / its MMAs done
 //   s_full[i]                S_i of the current key tile is in tensor memory
 //   p_full[i]                P_i written (and O_i rescaled) by the 128 softmax threads
 //   o_full[i] / o_empty[i]   O_i of an item complete / read out by the epilogue
 #pragma once
+
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -62,8 +64,12 @@ struct PrefillCfg {
   static constexpr int BN = 128;  // keys per K/V tile
   static constexpr int DCH = D / 64;  // 128-byte swizzle atoms across d
   static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (bf16)
+  // Q is double-buffered (the next item's Q loads while the current item
+  // runs) when shared memory allows: at d=64 always; at d=128 the K/V ring
+  // would have to shrink to three stages, so one Q buffer is kept there.
+  static constexpr int QBUF = (D == 128) ? 1 : 2;
   static constexpr int STAGES = (D == 128) ? 4 : 8;
-  static constexpr int RING_OFF = 2 * TILE_BYTES;
+  static constexpr int RING_OFF = QBUF * 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
   static constexpr int THREADS = 384;
@@ -129,9 +135,9 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::RING_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;                // [2]
-  uint64_t* q_empty = q_full + 2;         // [2]
-  uint64_t* kv_full = q_empty + 2;        // [STAGES]
+  uint64_t* q_full = bars;                   // [QBUF][2]
+  uint64_t* q_empty = q_full + 2 * C::QBUF;  // [QBUF][2]
+  uint64_t* kv_full = q_empty + 2 * C::QBUF; // [STAGES]
   uint64_t* kv_empty = kv_full + STAGES;  // [STAGES]
   uint64_t* s_full = kv_empty + STAGES;   // [2]
   uint64_t* p_full = s_full + 2;          // [2]
@@ -147,9 +153,11 @@ __global__ void __launch_bounds__(384, 1)
   const int N = p.N;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2 * C::QBUF; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
@@ -192,14 +200,16 @@ __global__ void __launch_bounds__(384, 1)
         const PrefillItem it = prefill_item_info(p, item);
         // Q tile i of this item, once the last S MMA of the previous item
         // has read the buffer.
+        const int qs = k % C::QBUF, qr = k / C::QBUF;  // Q buffer and its reuse count
         for (int i = 0; i < 2 && ok; ++i) {
-          if (k > 0 && !(ok = mbar_wait(&q_empty[i], (k - 1) & 1, &g_prefill_status,
-                                        kStatusProducer)))
+          uint64_t* qf = &q_full[qs * 2 + i];
+          if (qr > 0 && !(ok = mbar_wait(&q_empty[qs * 2 + i], (qr - 1) & 1, &g_prefill_status,
+                                         kStatusProducer)))
             break;
-          mbar_arrive_expect_tx(&q_full[i], C::TILE_BYTES);
+          mbar_arrive_expect_tx(qf, C::TILE_BYTES);
           for (int cc = 0; cc < C::DCH; ++cc)
-            tma_load_4d(sQ + i * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, &q_full[i], cc * 64,
-                        it.h, it.qb * 256 + i * 128, it.b);
+            tma_load_4d(sQ + (qs * 2 + i) * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, qf,
+                        cc * 64, it.h, it.qb * 256 + i * 128, it.b);
         }
         const int nloads = 2 * (it.J1 - it.J0 + 1);  // K_j, V_j alternate in the ring
         for (int u = 0; u < nloads && ok; ++u, ++issued) {
@@ -220,9 +230,10 @@ __global__ void __launch_bounds__(384, 1)
       // the normal path, where the MMA warp already consumed them all).
       for (int u = max(0, issued - STAGES); u < issued; ++u)
         mbar_wait(&kv_full[u % STAGES], (u / STAGES) & 1, &g_prefill_status, kStatusProducer);
-      if (k > 0)
+      for (int kk = max(0, k - C::QBUF); kk < k; ++kk)
         for (int i = 0; i < 2; ++i)
-          mbar_wait(&q_full[i], (k - 1) & 1, &g_prefill_status, kStatusProducer);
+          mbar_wait(&q_full[(kk % C::QBUF) * 2 + i], (kk / C::QBUF) & 1, &g_prefill_status,
+                    kStatusProducer);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -240,8 +251,9 @@ __global__ void __launch_bounds__(384, 1)
     };
 
     // S_i = Q_i K^T: K-major operands, 16 elements of d per instruction.
+    int qs = 0;  // Q buffer of the current item
     auto issue_S = [&](int i, int stage) {
-      const uint64_t a0 = dq0 + static_cast<uint64_t>((i * C::TILE_BYTES) >> 4);
+      const uint64_t a0 = dq0 + static_cast<uint64_t>(((qs * 2 + i) * C::TILE_BYTES) >> 4);
       const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -266,16 +278,17 @@ __global__ void __launch_bounds__(384, 1)
     for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
          item = prefill_item(c, ++k, G)) {
       const PrefillItem it = prefill_item_info(p, item);
-      for (int i = 0; i < 2 && ok; ++i) ok = wait(&q_full[i], k & 1);
+      qs = k % C::QBUF;
+      for (int i = 0; i < 2 && ok; ++i) ok = wait(&q_full[qs * 2 + i], (k / C::QBUF) & 1);
       if (ok) ok = wait(&kv_full[t0 % STAGES], (t0 / STAGES) & 1);
       if (!ok) break;
       tc_fence_after();
       for (int i = 0; i < 2; ++i) {
         if (it.act[i] && it.J0 >= it.jlo[i] && it.J0 <= it.jhi[i]) {
           issue_S(i, t0 % STAGES);
-          if (it.jhi[i] == it.J0) umma_commit_warp(&q_empty[i]);
+          if (it.jhi[i] == it.J0) umma_commit_warp(&q_empty[qs * 2 + i]);
         } else if (!it.act[i]) {
-          umma_commit_warp(&q_empty[i]);  // no S MMA reads this Q tile
+          umma_commit_warp(&q_empty[qs * 2 + i]);  // no S MMA reads this Q tile
         }
       }
       umma_commit_warp(&kv_empty[t0 % STAGES]);
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
               k_ready = true;
             }
             issue_S(i, sk);
-            if (j + 1 == it.jhi[i]) umma_commit_warp(&q_empty[i]);
+            if (j + 1 == it.jhi[i]) umma_commit_warp(&q_empty[qs * 2 + i]);
           }
         }
         if (!ok) break;
@@ -368,56 +381,99 @@ __global__ void __launch_bounds__(384, 1)
         const bool need_mask =
             (kv0 + BN > N) || (causal && kv0 + BN - 1 > r0) ||
             (window >= 0 && (r0 + 127 - kv0 > window || (!causal && kv0 + BN - 1 - r0 > window)));
-        if (need_mask) {
-#pragma unroll
-          for (int cc = 0; cc < 128; ++cc) {
-            const int key = kv0 + cc;
-            bool vis = key < N;
-            if (causal) vis = vis && key <= row;
-            if (window >= 0) vis = vis && (row - key <= window) && (causal || key - row <= window);
-            if (!vis) s[cc] = -INFINITY;
-          }
-        }
-        // row maximum: four independent chains of three-input max
-        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int cc = 0; cc < 128; cc += 8)
-#pragma unroll
-          for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
-        const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-        const float m_new = fmaxf(m_ref, mx * sl2);
-        const bool resc = m_new > m_ref + kRescaleThreshold;
+        // One tile of the online softmax; MASKED is a compile-time flag so that
+        // the common, unmasked tile runs straight-line code.
+        bool resc = false;
         float alpha = 1.f;
-        if (resc) {
-          alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
-          m_ref = m_new;
-          l *= alpha;
-        }
-        const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
-        // in four packed partial sums, bf16 pairs into tensor memory
-        const float2 sl2x2 = make_float2(sl2, sl2);
-        const float2 nmu2 = make_float2(neg_mu, neg_mu);
-        float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
+        auto tile = [&](auto masked_tag) {
+          constexpr bool MASKED = decltype(masked_tag)::value;
+          // Columns [lo_c, hi_c] of this tile are visible to this row.
+          // Masking works on 32-column chunks, classified for the whole warp:
+          // visible in every row (left alone), masked in every row ("dead":
+          // no max, no exp, P = 0), or mixed (masked column by column).
+          bool dead[4] = {false, false, false, false};
+          if (MASKED) {
+            int lo = 0, hi = N - 1;
+            if (causal) hi = min(hi, row);
+            if (window >= 0) {
+              lo = max(lo, row - window);
+              if (!causal) hi = min(hi, row + window);
+            }
+            const int lo_c = lo - kv0, hi_c = hi - kv0;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
+            for (int q = 0; q < 4; ++q) {
+              if (__all_sync(0xffffffffu, lo_c <= 32 * q && hi_c >= 32 * q + 31)) continue;
+              dead[q] = __all_sync(0xffffffffu, hi_c < 32 * q || lo_c > 32 * q + 31);
+              if (dead[q]) continue;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 x =
-                ffma2(make_float2(s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1]), sl2x2, nmu2);
-            const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            lacc[e & 3] = fadd2(lacc[e & 3], pe);
-            pk[e] = pack_bf16x2(pe.x, pe.y);
+              for (int e = 0; e < 32; ++e) {
+                const int cc = 32 * q + e;
+                s[cc] = (cc >= lo_c && cc <= hi_c) ? s[cc] : -INFINITY;
+              }
+            }
           }
-          tmem_st16(tS + cc * 16, pk);
-        }
-        {
+          // row maximum: independent chains of three-input max
+          float mx = -INFINITY;
+          if (MASKED) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (dead[q]) continue;
+              float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                m0 = fmax3(m0, s[32 * q + e], s[32 * q + e + 1]);
+                m1 = fmax3(m1, s[32 * q + e + 2], s[32 * q + e + 3]);
+              }
+              mx = fmax3(mx, m0, m1);
+            }
+          } else {
+            float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 8)
+#pragma unroll
+              for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
+            mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
+          }
+          const float m_new = fmaxf(m_ref, mx * sl2);
+          resc = m_new > m_ref + kRescaleThreshold;
+          if (resc) {
+            alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
+            m_ref = m_new;
+            l *= alpha;
+          }
+          const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+          // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row
+          // sum in four packed partial sums, bf16 pairs into tensor memory
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 nmu2 = make_float2(neg_mu, neg_mu);
+          float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
+            if (MASKED && dead[q]) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float2 x =
+                    ffma2(make_float2(s[q * 32 + 2 * e], s[q * 32 + 2 * e + 1]), sl2x2, nmu2);
+                const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                lacc[e & 3] = fadd2(lacc[e & 3], pe);
+                pk[e] = pack_bf16x2(pe.x, pe.y);
+              }
+            }
+            tmem_st16(tS + q * 16, pk);
+          }
           const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
           const float2 t = fadd2(a, b2);
           l += t.x + t.y;
-        }
+        };
+        if (need_mask)
+          tile(std::true_type{});
+        else
+          tile(std::false_type{});
         // Rescale this row of O (only rows whose maximum moved; the previous
         // P V of this tile is complete because S_i(j) was committed after it).
         if (j > it.jlo[i] && __any_sync(0xffffffffu, resc)) {
