@@ -38,8 +38,6 @@
 //   o_full[i] / o_empty[i]   O_i of an item complete / read out by the epilogue
 #pragma once
 
-#include <type_traits>
-
 #include "ptx.cuh"
 
 namespace b300 {
@@ -381,99 +379,69 @@ __global__ void __launch_bounds__(384, 1)
         const bool need_mask =
             (kv0 + BN > N) || (causal && kv0 + BN - 1 > r0) ||
             (window >= 0 && (r0 + 127 - kv0 > window || (!causal && kv0 + BN - 1 - r0 > window)));
-        // One tile of the online softmax; MASKED is a compile-time flag so that
-        // the common, unmasked tile runs straight-line code.
-        bool resc = false;
-        float alpha = 1.f;
-        auto tile = [&](auto masked_tag) {
-          constexpr bool MASKED = decltype(masked_tag)::value;
-          // Columns [lo_c, hi_c] of this tile are visible to this row.
-          // Masking works on 32-column chunks, classified for the whole warp:
-          // visible in every row (left alone), masked in every row ("dead":
-          // no max, no exp, P = 0), or mixed (masked column by column).
-          bool dead[4] = {false, false, false, false};
-          if (MASKED) {
-            int lo = 0, hi = N - 1;
-            if (causal) hi = min(hi, row);
-            if (window >= 0) {
-              lo = max(lo, row - window);
-              if (!causal) hi = min(hi, row + window);
-            }
-            const int lo_c = lo - kv0, hi_c = hi - kv0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (__all_sync(0xffffffffu, lo_c <= 32 * q && hi_c >= 32 * q + 31)) continue;
-              dead[q] = __all_sync(0xffffffffu, hi_c < 32 * q || lo_c > 32 * q + 31);
-              if (dead[q]) continue;
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int cc = 32 * q + e;
-                s[cc] = (cc >= lo_c && cc <= hi_c) ? s[cc] : -INFINITY;
-              }
-            }
+        // Mask: columns [lo_c, hi_c] of this tile are visible to this row.
+        // Each 32-column chunk that is visible in every row of the warp is
+        // skipped; the others get a per-column select.  One code path serves
+        // masked and unmasked tiles (the kernel's instructions must stay
+        // within the instruction cache).
+        if (need_mask) {
+          int lo = 0, hi = N - 1;
+          if (causal) hi = min(hi, row);
+          if (window >= 0) {
+            lo = max(lo, row - window);
+            if (!causal) hi = min(hi, row + window);
           }
-          // row maximum: independent chains of three-input max
-          float mx = -INFINITY;
-          if (MASKED) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (dead[q]) continue;
-              float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-              for (int e = 0; e < 32; e += 4) {
-                m0 = fmax3(m0, s[32 * q + e], s[32 * q + e + 1]);
-                m1 = fmax3(m1, s[32 * q + e + 2], s[32 * q + e + 3]);
-              }
-              mx = fmax3(mx, m0, m1);
-            }
-          } else {
-            float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int cc = 0; cc < 128; cc += 8)
-#pragma unroll
-              for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
-            mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-          }
-          const float m_new = fmaxf(m_ref, mx * sl2);
-          resc = m_new > m_ref + kRescaleThreshold;
-          if (resc) {
-            alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
-            m_ref = m_new;
-            l *= alpha;
-          }
-          const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
-          // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row
-          // sum in four packed partial sums, bf16 pairs into tensor memory
-          const float2 sl2x2 = make_float2(sl2, sl2);
-          const float2 nmu2 = make_float2(neg_mu, neg_mu);
-          float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                            make_float2(0.f, 0.f)};
+          const int lo_c = lo - kv0, hi_c = hi - kv0;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t pk[16];
-            if (MASKED && dead[q]) {
+            if (__all_sync(0xffffffffu, lo_c <= 32 * q && hi_c >= 32 * q + 31)) continue;
 #pragma unroll
-              for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const float2 x =
-                    ffma2(make_float2(s[q * 32 + 2 * e], s[q * 32 + 2 * e + 1]), sl2x2, nmu2);
-                const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                lacc[e & 3] = fadd2(lacc[e & 3], pe);
-                pk[e] = pack_bf16x2(pe.x, pe.y);
-              }
+            for (int e = 0; e < 32; ++e) {
+              const int cc = 32 * q + e;
+              s[cc] = (cc >= lo_c && cc <= hi_c) ? s[cc] : -INFINITY;
             }
-            tmem_st16(tS + q * 16, pk);
           }
+        }
+        // row maximum: four independent chains of three-input max
+        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int cc = 0; cc < 128; cc += 8)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
+        const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        const bool resc = m_new > m_ref + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
+        // in four packed partial sums, bf16 pairs into tensor memory
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 nmu2 = make_float2(neg_mu, neg_mu);
+        float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 x =
+                ffma2(make_float2(s[q * 32 + 2 * e], s[q * 32 + 2 * e + 1]), sl2x2, nmu2);
+            const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            lacc[e & 3] = fadd2(lacc[e & 3], pe);
+            pk[e] = pack_bf16x2(pe.x, pe.y);
+          }
+          tmem_st16(tS + q * 16, pk);
+        }
+        {
           const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
           const float2 t = fadd2(a, b2);
           l += t.x + t.y;
-        };
-        if (need_mask)
-          tile(std::true_type{});
-        else
-          tile(std::false_type{});
+        }
         // Rescale this row of O (only rows whose maximum moved; the previous
         // P V of this tile is complete because S_i(j) was committed after it).
         if (j > it.jlo[i] && __any_sync(0xffffffffu, resc)) {
