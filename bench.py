@@ -67,11 +67,14 @@ def load_peaks():
 
 
 def kernel_source_sha():
-    """Hash of the kernel sources; a stored ncu traffic figure is used only if
-    it was taken from the same sources."""
+    """Hash of the device-code sources (the .cuh files that define the
+    kernels); a stored ncu traffic figure is used only if it was taken from
+    the same device code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, PKG, "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not f.endswith(".cuh"):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -294,26 +297,56 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- timing
-def time_launches(fn, steps: int, warmup: int, dist: Dist, clocks=None):
+LAST_TIMING = {}  # how the last time_launches call timed (mode, host enqueue time per call)
+
+
+def time_launches(fn, steps: int, warmup: int, dist: Dist, clocks=None, graph: bool = True):
     """Average device time of one call of ``fn`` (ms), CUDA events on the
-    current stream, max over ranks."""
+    current stream, max over ranks.
+
+    With ``graph`` the call is captured once in a CUDA graph (after the
+    warm-up) and the timed region replays it ``steps`` times: each replay runs
+    exactly the kernels of one call, without the per-call host work (argument
+    checks, tensor-map encoding, ctypes), which for short kernels would
+    otherwise leave the GPU idle between launches.  If capture fails the
+    calls are timed as plain launches."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    run = fn
+    mode = "plain launches"
+    if graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    fn()
+            torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+            torch.cuda.synchronize()
+            run = g.replay
+            mode = "cuda graph replay (one call per replay)"
+        except Exception as e:  # capture not possible: time plain launches
+            mode = f"plain launches (graph capture failed: {type(e).__name__})"
     dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     start.record()
     for _ in range(steps):
-        fn()
+        run()
     end.record()
+    t_enq = time.perf_counter()
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     if clocks is not None:
         clocks.window(t0, t1)
     dist.barrier()
+    LAST_TIMING.clear()
+    LAST_TIMING.update({"mode": mode, "host_enqueue_ms_per_call": round((t_enq - t0) / steps * 1e3, 4)})
     return dist.max(start.elapsed_time(end) / steps)
 
 
@@ -356,6 +389,10 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             ms = time_launches(step, steps, warmup, dist, clocks)
     else:
         ms = time_launches(step, steps, warmup, dist)
+    timing = dict(LAST_TIMING)
+    ms_plain = time_launches(step, steps, warmup, dist, graph=False)
+    timing["plain_launch_ms"] = round(ms_plain, 5)
+    timing["plain_host_enqueue_ms_per_call"] = LAST_TIMING["host_enqueue_ms_per_call"]
     assert fa.device_status() == 0, fa.last_error()
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -365,7 +402,7 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
     rf["frac_of_sustained"] = round(tflops / peaks.get("bf16_tflops_sustained", peak), 4)
     io_bytes = (q.numel() + k.numel() + v.numel()) * 2 + o.numel() * o.element_size() + lse.numel() * 4
     return {"ms": ms, "tflops": tflops, "flops": flops, "roofline": rf, "io_bytes": io_bytes,
-            "launches_per_step": 1}
+            "launches_per_step": 1, "timing": timing}
 
 
 def decode_case(w, dev):
@@ -403,6 +440,7 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             ms_full = time_launches(full, steps, warmup, dist, clocks)
     else:
         ms_full = time_launches(full, steps, warmup, dist)
+    timing = dict(LAST_TIMING)
     ms_part = time_launches(partials, steps, warmup, dist)
     ms_comb = time_launches(combine, steps, warmup, dist)
     assert fa.device_status() == 0, fa.last_error()
@@ -417,7 +455,7 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             "kv_bytes": kv_bytes, "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
             "frac_of_nameplate_8tbs": round(gbs / NAMEPLATE_HBM_GBS, 4),
             "kernels": {"decode_partial_kernel_ms": ms_part, "lse_combine_kernel_ms": ms_comb},
-            "launches_per_call": 2, "roofline": rf,
+            "launches_per_call": 2, "roofline": rf, "timing": timing,
             "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lmax": w.N, "d": w.d,
                        "num_splits": w.num_splits,
                        "kv_len": "uniform [%d, %d]" % (w.kv_len_lo, w.kv_len_hi)
@@ -659,6 +697,8 @@ def main():
     }
     if w.kind == "decode":
         line["kernels"] = main_res["kernels"]
+    if "timing" in main_res:
+        line["timing"] = main_res["timing"]
     line["config"]["parallelism"] = f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 10))
@@ -679,7 +719,7 @@ def main():
                               peak_kind)
             extra[name] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
                            "ms_per_call": r["ms"], "roofline": r["roofline"],
-                           "config": workload_config(wn)}
+                           "timing": r["timing"], "config": workload_config(wn)}
         line["extra"] = extra
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget) if w.kind == "prefill" else \

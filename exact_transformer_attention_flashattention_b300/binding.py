@@ -24,6 +24,8 @@ BF16, F32 = 0, 1
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P,
+                             _I]),
     "attn_decode_chunk": (_I, [_I, _I]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ,
@@ -114,6 +116,31 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = -1, scale: float | Non
     _check(_lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
                          int(bool(causal)), int(window), float(scale), _stream(stream),
                          _odtype(out.dtype)))
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, window: int = -1,
+                    scale: float | None = None, out=None, lse=None, out_dtype=torch.bfloat16,
+                    stream=None):
+    """Prefill over sequences packed back to back.  q [T,Hq,d], k/v [T,Hkv,d] bf16,
+    cu_seqlens int32 [S+1] on the device -> (O [T,Hq,d], LSE [Hq,T])."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((T, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    S = cu_seqlens.numel() - 1
+    _check(_lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                                S, T, int(max_seqlen), Hq, Hkv, d, int(bool(causal)), int(window),
+                                float(scale), _stream(stream), _odtype(out.dtype)))
     return out, lse
 
 

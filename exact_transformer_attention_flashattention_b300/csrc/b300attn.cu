@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <string>
 
 #include "b300attn.h"
@@ -70,11 +72,39 @@ int make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   return B300ATTN_OK;
 }
 
+// 3-D bf16 tensor map over a row-major [d2][d1][d0] array (d0 contiguous).
+int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swizzle,
+                const char* name) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                static_cast<int>(r));
+  return B300ATTN_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit, once per (kernel, device).
 template <typename K>
 int set_smem(K kernel, int bytes) {
-  const cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return B300ATTN_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  done.insert(key);
   return B300ATTN_OK;
 }
 
@@ -100,27 +130,30 @@ int sm_count(int* out) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// `max_items` bounds the number of work items (exact for the dense layout).
 template <int D>
 int launch_prefill(const void* q, const void* k, const void* v, const PrefillParams& p,
-                   cudaStream_t stream) {
+                   long long max_items, cudaStream_t stream) {
   using C = PrefillCfg<D>;
   CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_map_4d(&tq, q, D, p.Hq, p.N, p.B, 64, 1, C::BM, 1,
+  // q, k, v seen as [rows, heads, d]; tiles of 128 rows x 64 elements of d
+  if ((rc = make_map_3d(&tq, q, D, p.Hq, p.total_rows, 64, 1, C::BM,
                         CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
     return rc;
-  if ((rc = make_map_4d(&tk, k, D, p.Hkv, p.N, p.B, 64, 1, C::BN, 1,
+  if ((rc = make_map_3d(&tk, k, D, p.Hkv, p.total_rows, 64, 1, C::BN,
                         CU_TENSOR_MAP_SWIZZLE_128B, "k")) != B300ATTN_OK)
     return rc;
-  if ((rc = make_map_4d(&tv, v, D, p.Hkv, p.N, p.B, 64, 1, C::BN, 1,
+  if ((rc = make_map_3d(&tv, v, D, p.Hkv, p.total_rows, 64, 1, C::BN,
                         CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
     return rc;
-  if ((rc = set_smem(prefill_kernel<D>, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
+  auto kernel = p.cu_seqlens ? prefill_kernel<D, true> : prefill_kernel<D, false>;
+  if ((rc = set_smem(kernel, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
   int sms = 0;
   if ((rc = sm_count(&sms)) != B300ATTN_OK) return rc;
   // persistent: one CTA per SM (the kernel's shared memory admits no second one)
-  const int grid = std::min(p.n_items, sms);
-  prefill_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  const int grid = static_cast<int>(std::min<long long>(max_items, sms));
+  kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return B300ATTN_OK;
@@ -305,9 +338,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!std::isfinite(scale) || scale < 0.f)
     return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
                 static_cast<double>(scale));
+  if (static_cast<long long>(B) * N > 0x7fffffffLL)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "B*N=%lld rows exceed 2^31-1",
+                static_cast<long long>(B) * N);
   PrefillParams p;
   p.o = o;
   p.lse = lse;
+  p.cu_seqlens = nullptr;
+  p.num_seqs = B;
+  p.total_rows = B * N;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -321,7 +360,55 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   const long long items = static_cast<long long>(p.nqb) * Hq * B;
   if (items > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
   p.n_items = static_cast<int>(items);
-  return d == 128 ? launch_prefill<128>(q, k, v, p, stream) : launch_prefill<64>(q, k, v, p, stream);
+  return d == 128 ? launch_prefill<128>(q, k, v, p, p.n_items, stream)
+                  : launch_prefill<64>(q, k, v, p, p.n_items, stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int num_seqs, int total_rows, int max_seqlen, int Hq,
+                    int Hkv, int d, int causal, int window, float scale, cudaStream_t stream,
+                    int o_dtype) {
+  if (num_seqs < 0 || total_rows < 0 || max_seqlen < 0 || Hq < 0 || Hkv < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size");
+  if (num_seqs == 0 || total_rows == 0 || max_seqlen == 0 || Hq == 0) return B300ATTN_OK;
+  if (num_seqs > kMaxVarlenSeqs)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "num_seqs=%d exceeds %d sequences per launch", num_seqs,
+                kMaxVarlenSeqs);
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(B300ATTN_ERR_INVALID, "cu_seqlens must be 4-byte aligned");
+  if (causal != 0 && causal != 1) return fail(B300ATTN_ERR_INVALID, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
+                static_cast<double>(scale));
+  PrefillParams p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.num_seqs = num_seqs;
+  p.total_rows = total_rows;
+  p.B = 0;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = 0;
+  p.causal = causal;
+  p.window = window < 0 ? -1 : window;
+  p.o_f32 = o_dtype == B300ATTN_F32;
+  p.nqb = 0;
+  p.n_items = 0;  // counted on the device from cu_seqlens
+  p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
+  const long long bound =
+      static_cast<long long>(num_seqs) * ((std::min(max_seqlen, total_rows) + 255) / 256) * Hq;
+  if (bound > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
+  return d == 128 ? launch_prefill<128>(q, k, v, p, bound, stream)
+                  : launch_prefill<64>(q, k, v, p, bound, stream);
 }
 
 int attn_decode_chunk(int max_kv_len, int num_splits) {

@@ -18,7 +18,7 @@
 //
 // CTA layout (384 threads):
 //   warp 0      TMA producer: Q tiles of each item, then K_j, V_j into a STAGES-deep ring
-//   warp 1      MMA issuer (lane 0): S_i = Q_i K_j^T, O_i += P_i V_j
+//   warp 1      MMA issuer (whole warp, one elected lane): S_i = Q_i K_j^T, O_i += P_i V_j
 //   warp 2      tensor-memory allocator
 //   warp 3      idle
 //   warps 4-7   softmax + epilogue for Q tile 0 (rows  0..127 of the block)
@@ -46,13 +46,25 @@ __device__ unsigned int g_prefill_status;  // OR of kStatus* bits (bounded waits
 
 constexpr unsigned kStatusProducer = 1u, kStatusMma = 2u, kStatusSoftmax = 4u;
 
+// Maximum number of sequences of one variable-length launch (the per-CTA item
+// table lives in shared memory).
+constexpr int kMaxVarlenSeqs = 4096;
+
+// Two layouts share one kernel.  Dense: B sequences of N tokens,
+// q [B, N, Hq, d], LSE [B, Hq, N].  Variable length: `cu_seqlens[0..num_seqs]`
+// (int32, device) holds the first token of each sequence in packed
+// q [T, Hq, d], k/v [T, Hkv, d] (T = total_rows), LSE [Hq, T].  Either way the
+// tensor maps see a [rows, heads, d] array and every item carries its
+// sequence's first row and length.
 struct PrefillParams {
   void* o;
   float* lse;
-  int B, Hq, Hkv, N;
+  const int* cu_seqlens;  // NULL: dense layout
+  int B, Hq, Hkv, N;      // dense: batch and sequence length
+  int num_seqs, total_rows;
   int causal, window, o_f32;
-  int nqb;           // number of 256-row query blocks
-  int n_items;       // nqb * B * Hq
+  int nqb;           // dense: number of 256-row query blocks per sequence
+  int n_items;       // dense: nqb * B * Hq (variable length: counted on the device)
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -69,7 +81,10 @@ struct PrefillCfg {
   static constexpr int STAGES = (D == 128) ? 4 : 8;
   static constexpr int RING_OFF = QBUF * 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
+  // + barriers and the TMEM address (512 B), the variable-length item table
+  // (kMaxVarlenSeqs + 1 ints), alignment slack
+  static constexpr int TABLE_OFF = BAR_OFF + 512;
+  static constexpr int SMEM_BYTES = TABLE_OFF + (kMaxVarlenSeqs + 1) * 4 + 1024;
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(BM == BN, "Q and K/V tiles share one byte layout");
@@ -80,31 +95,67 @@ __device__ __forceinline__ int prefill_item(int c, int k, int G) {
   return (k & 1) ? k * G + (G - 1 - c) : k * G + c;
 }
 
-// What one work item covers: query block qb of (b, h), and the key-tile
-// range [jlo[i], jhi[i]] of each of its two Q tiles.
+// What one work item covers: query block qb of head h of sequence b (whose
+// tokens are rows [base, base + n) of the [rows, heads, d] view), and the
+// key-tile range [jlo[i], jhi[i]] of each of its two Q tiles.
 struct PrefillItem {
   int qb, b, h, hk;
+  int base, n;
   int jlo[2], jhi[2];
   bool act[2];
   int J0, J1;
 };
 
-__device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p, int item) {
+// First row and length of variable-length sequence s, clamped so that every
+// row the kernel touches lies inside [0, total_rows) whatever cu_seqlens holds.
+__device__ __forceinline__ void varlen_seq(const PrefillParams& p, int s, int& base, int& n) {
+  const int a = min(max(p.cu_seqlens[s], 0), p.total_rows);
+  const int e = min(max(p.cu_seqlens[s + 1], a), p.total_rows);
+  base = a;
+  n = e - a;
+}
+
+// `table[s]` (s = 0..num_seqs) is the number of items of sequences 0..s-1
+// (variable-length layout only).
+template <bool VARLEN>
+__device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p, int item,
+                                                         const int* table) {
   constexpr int BN = 128;
   PrefillItem it;
-  const int BH = p.B * p.Hq;
-  int bh;
-  if (p.causal) {  // heaviest query blocks first
-    it.qb = p.nqb - 1 - item / BH;
-    bh = item % BH;
-  } else {  // all blocks of one head together: they share its K/V in L2
-    it.qb = item % p.nqb;
-    bh = item / p.nqb;
+  if constexpr (VARLEN) {
+    int lo = 0, hi = p.num_seqs - 1;  // last s with table[s] <= item
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (table[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    it.b = lo;
+    varlen_seq(p, lo, it.base, it.n);
+    const int nqb = (it.n + 255) / 256;
+    const int local = item - table[lo];
+    if (p.causal) {  // heaviest query blocks of the sequence first
+      it.qb = nqb - 1 - local / p.Hq;
+      it.h = local % p.Hq;
+    } else {
+      it.qb = local % nqb;
+      it.h = local / nqb;
+    }
+  } else {
+    const int BH = p.B * p.Hq;
+    int bh;
+    if (p.causal) {  // heaviest query blocks first
+      it.qb = p.nqb - 1 - item / BH;
+      bh = item % BH;
+    } else {  // all blocks of one head together: they share its K/V in L2
+      it.qb = item % p.nqb;
+      bh = item / p.nqb;
+    }
+    it.b = bh / p.Hq;
+    it.h = bh % p.Hq;
+    it.base = it.b * p.N;
+    it.n = p.N;
   }
-  it.b = bh / p.Hq;
-  it.h = bh % p.Hq;
   it.hk = it.h / (p.Hq / p.Hkv);
-  const int N = p.N;
+  const int N = it.n;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int r0 = it.qb * 256 + i * 128;
@@ -120,7 +171,9 @@ __device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p,
   return it;
 }
 
-template <int D>
+// VARLEN selects the layout at compile time, so that the dense launch carries
+// none of the variable-length bookkeeping.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -143,12 +196,51 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* o_empty = o_full + 2;         // [2]
   uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* table = reinterpret_cast<int*>(smem + C::TABLE_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int c = blockIdx.x;
-  const int N = p.N;
+
+  // Variable length: items per sequence (query blocks x heads), prefix-summed
+  // into the shared table by a block-wide scan.
+  int n_items = p.n_items;
+  if constexpr (VARLEN) {
+    constexpr int PER = (kMaxVarlenSeqs + C::THREADS - 1) / C::THREADS;
+    int cnt[PER];
+    int mine = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int s = threadIdx.x * PER + u;
+      cnt[u] = 0;
+      if (s < p.num_seqs) {
+        int b0, n0;
+        varlen_seq(p, s, b0, n0);
+        cnt[u] = (n0 + 255) / 256 * p.Hq;
+      }
+      mine += cnt[u];
+    }
+    int incl = mine;  // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __shared__ int warp_sum[C::THREADS / 32];
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int before = incl - mine;
+    for (int w = 0; w < warp; ++w) before += warp_sum[w];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int s = threadIdx.x * PER + u;
+      if (s <= p.num_seqs) table[s] = before;
+      before += cnt[u];
+    }
+    __syncthreads();
+    n_items = table[p.num_seqs];
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * C::QBUF; ++i) {
@@ -183,19 +275,19 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   // Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup
-  // 0 (producer, MMA, allocator, idle) gives back to 64 and the two softmax
-  // warpgroups take 216: 128 x 64 + 256 x 216 = 63488 <= 64512.
+  // 0 (producer, MMA issuer, allocator, idle) gives back to 136 and the two softmax
+  // warpgroups take 184: 128 x 136 + 256 x 184 = 64512.
   if (warp < 4) {
-  setmaxnreg_dec<120>();
+  setmaxnreg_dec<136>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
       bool ok = true;
       int issued = 0;  // K/V ring loads issued so far (all items)
       int k = 0;       // items of this CTA started
-      for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+      for (int item = prefill_item(c, 0, G); item < n_items && ok;
            item = prefill_item(c, ++k, G)) {
-        const PrefillItem it = prefill_item_info(p, item);
+        const PrefillItem it = prefill_item_info<VARLEN>(p, item, table);
         // Q tile i of this item, once the last S MMA of the previous item
         // has read the buffer.
         const int qs = k % C::QBUF, qr = k / C::QBUF;  // Q buffer and its reuse count
@@ -206,8 +298,8 @@ __global__ void __launch_bounds__(384, 1)
             break;
           mbar_arrive_expect_tx(qf, C::TILE_BYTES);
           for (int cc = 0; cc < C::DCH; ++cc)
-            tma_load_4d(sQ + (qs * 2 + i) * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, qf,
-                        cc * 64, it.h, it.qb * 256 + i * 128, it.b);
+            tma_load_3d(sQ + (qs * 2 + i) * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, qf,
+                        cc * 64, it.h, it.base + it.qb * 256 + i * 128);
         }
         const int nloads = 2 * (it.J1 - it.J0 + 1);  // K_j, V_j alternate in the ring
         for (int u = 0; u < nloads && ok; ++u, ++issued) {
@@ -220,8 +312,8 @@ __global__ void __launch_bounds__(384, 1)
           const int j = it.J0 + u / 2;
           const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
           for (int cc = 0; cc < C::DCH; ++cc)
-            tma_load_4d(sRing + s * C::TILE_BYTES + cc * (BN * 128), tm, &kv_full[s], cc * 64,
-                        it.hk, j * BN, it.b);
+            tma_load_3d(sRing + s * C::TILE_BYTES + cc * (BN * 128), tm, &kv_full[s], cc * 64,
+                        it.hk, it.base + j * BN);
         }
       }
       // Every issued copy has landed before the CTA may exit (a no-op wait on
@@ -273,9 +365,9 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     int t0 = 0;  // ring position of this item's first load (K_J0)
     int k = 0;
-    for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+    for (int item = prefill_item(c, 0, G); item < n_items && ok;
          item = prefill_item(c, ++k, G)) {
-      const PrefillItem it = prefill_item_info(p, item);
+      const PrefillItem it = prefill_item_info<VARLEN>(p, item, table);
       qs = k % C::QBUF;
       for (int i = 0; i < 2 && ok; ++i) ok = wait(&q_full[qs * 2 + i], (k / C::QBUF) & 1);
       if (ok) ok = wait(&kv_full[t0 % STAGES], (t0 / STAGES) & 1);
@@ -298,7 +390,9 @@ __global__ void __launch_bounds__(384, 1)
         const bool has_next = j < it.J1;
         const int sk = (t + 1) % STAGES;
         bool k_ready = false;
-        for (int i = 0; i < 2 && ok; ++i) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (!ok) break;
           if (it.act[i] && j >= it.jlo[i] && j <= it.jhi[i]) {
             if (!(ok = wait(&p_full[i], pcnt[i] & 1))) break;
             ++pcnt[i];
@@ -335,7 +429,7 @@ __global__ void __launch_bounds__(384, 1)
     wait(mma_done, 0);
   }
   } else {
-    setmaxnreg_inc<192>();
+    setmaxnreg_inc<184>();
     // ================================================================ softmax
     const int i = (warp - 4) >> 2;   // Q tile of this warpgroup
     const int quarter = warp & 3;    // tensor-memory lane quarter this warp may access
@@ -350,15 +444,18 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t scnt = 0;  // s_full phases consumed
     uint32_t ocnt = 0;  // items in which this Q tile was active
     int k = 0;
-    for (int item = prefill_item(c, 0, G); item < p.n_items && ok;
+    for (int item = prefill_item(c, 0, G); item < n_items && ok;
          item = prefill_item(c, ++k, G)) {
-      const PrefillItem it = prefill_item_info(p, item);
-      if (!it.act[i]) continue;
+      const PrefillItem it = prefill_item_info<VARLEN>(p, item, table);
+      const bool act = i ? it.act[1] : it.act[0];  // selects: no run-time index into `it`
+      const int jlo = i ? it.jlo[1] : it.jlo[0];
+      const int jhi = i ? it.jhi[1] : it.jhi[0];
+      if (!act) continue;
       const int r0 = it.qb * 256 + i * 128;
       const int row = r0 + r;
       float m_ref = -INFINITY;  // base-2 running maximum actually used for P
       float l = 0.f;
-      for (int j = it.jlo[i]; j <= it.jhi[i]; ++j, ++scnt) {
+      for (int j = jlo; j <= jhi; ++j, ++scnt) {
         ok = mbar_wait(&s_full[i], scnt & 1, &g_prefill_status, kStatusSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -377,7 +474,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(u[cc][e]);
         const int kv0 = j * BN;
         const bool need_mask =
-            (kv0 + BN > N) || (causal && kv0 + BN - 1 > r0) ||
+            (kv0 + BN > it.n) || (causal && kv0 + BN - 1 > r0) ||
             (window >= 0 && (r0 + 127 - kv0 > window || (!causal && kv0 + BN - 1 - r0 > window)));
         // Mask: columns [lo_c, hi_c] of this tile are visible to this row.
         // Each 32-column chunk that is visible in every row of the warp is
@@ -385,7 +482,7 @@ __global__ void __launch_bounds__(384, 1)
         // masked and unmasked tiles (the kernel's instructions must stay
         // within the instruction cache).
         if (need_mask) {
-          int lo = 0, hi = N - 1;
+          int lo = 0, hi = it.n - 1;
           if (causal) hi = min(hi, row);
           if (window >= 0) {
             lo = max(lo, row - window);
@@ -444,7 +541,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         // Rescale this row of O (only rows whose maximum moved; the previous
         // P V of this tile is complete because S_i(j) was committed after it).
-        if (j > it.jlo[i] && __any_sync(0xffffffffu, resc)) {
+        if (j > jlo && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t w[32];
@@ -475,8 +572,8 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(&o_empty[i]);
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      if (row < N) {
-        const size_t orow = (static_cast<size_t>(it.b) * N + row) * p.Hq + it.h;
+      if (row < it.n) {
+        const size_t orow = (static_cast<size_t>(it.base) + row) * p.Hq + it.h;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           if (p.o_f32) {
@@ -505,7 +602,10 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
-        p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * N + row] =
+        const size_t li = VARLEN
+                              ? static_cast<size_t>(it.h) * p.total_rows + it.base + row
+                              : (static_cast<size_t>(it.b) * p.Hq + it.h) * it.n + row;
+        p.lse[li] =
             (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
     }

@@ -75,6 +75,33 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int o_dtype);
 
 /*
+ * attn_fwd_varlen -- prefill over a batch of sequences of different lengths,
+ * packed back to back along the token axis (no padding).
+ *
+ * The same tiled online-softmax attention as attn_fwd, applied within each
+ * sequence: sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]) and its
+ * queries see only its own keys (with the causal / window masks of attn_fwd,
+ * positions counted from the sequence's first token).  This is the
+ * "variable-length" form that long-document and serving workloads use
+ * ("FlashAttention" learn page, "The future of FlashAttention": variants for
+ * irregular and sliding-window attention).
+ *
+ *   q    bf16 [T, Hq, d]        k, v  bf16 [T, Hkv, d]      (T = total_rows)
+ *   o    [T, Hq, d], bf16 or f32 as o_dtype says;  lse  f32 [Hq, T]
+ *   cu_seqlens  int32 [num_seqs + 1], DEVICE, non-decreasing, cu_seqlens[0] = 0,
+ *               cu_seqlens[num_seqs] <= total_rows.  Values are clamped to
+ *               [0, total_rows] on the device (a decreasing entry gives an
+ *               empty sequence); rows outside every sequence are not written.
+ *   max_seqlen  upper bound of the sequence lengths (sizes the launch only).
+ *   1 <= num_seqs <= 4096; other arguments as for attn_fwd.
+ * Errors: INVALID, UNSUPPORTED (d, num_seqs > 4096), CUDA.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int num_seqs, int total_rows, int max_seqlen, int Hq,
+                    int Hkv, int d, int causal, int window, float scale, cudaStream_t stream,
+                    int o_dtype);
+
+/*
  * attn_decode_chunk -- keys per split used by attn_decode_splitkv:
  * ceil(max_kv_len / num_splits) rounded up to a multiple of 64.  Returns a
  * negative status on invalid arguments.

@@ -10,6 +10,7 @@ from .attention import (  # noqa: F401
     attention_band,
     attention_head,
     attention_rows,
+    attention_varlen,
     combine_rows,
     decode,
     lse_merge,

@@ -119,6 +119,28 @@ def attention(q, k, v, causal: bool = False, window: int = -1, scale: float | No
     return O, LSE
 
 
+def attention_varlen(q, k, v, cu_seqlens, causal: bool = False, window: int = -1,
+                     scale: float | None = None):
+    """Sequences packed back to back: sequence s owns rows [cu[s], cu[s+1]) of
+    q [T, Hq, d] and k/v [T, Hkv, d] and attends only within itself (masks
+    counted from its first row).  Returns O [T, Hq, d] and LSE [Hq, T]; rows
+    outside every sequence stay NaN."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, Hq, d = q.shape
+    cu = [int(x) for x in cu_seqlens]
+    O = np.full((T, Hq, v.shape[2]), np.nan)
+    LSE = np.full((Hq, T), np.nan)
+    for s in range(len(cu) - 1):
+        a, e = cu[s], cu[s + 1]
+        if e <= a:
+            continue
+        o_s, l_s = attention(q[None, a:e], k[None, a:e], v[None, a:e], causal=causal,
+                             window=window, scale=scale)
+        O[a:e] = o_s[0]
+        LSE[:, a:e] = l_s[0]
+    return O, LSE
+
+
 def attention_rows(q, k, v, b: int, h: int, rows, causal: bool = False, window: int = -1,
                    scale: float | None = None):
     """O and LSE for selected query rows of one (b, h): the same definition,

@@ -324,9 +324,30 @@ def pin_empty_rows(orc):
     _close(m[2], a[2], 1e-15, "identity merge o")
 
 
+def pin_varlen_bruteforce(orc, seed=13):
+    """Packed sequences: each sequence equals the brute-force loop on that
+    sequence alone (positions counted from its first row), and no row of one
+    sequence sees another's keys."""
+    rng = np.random.default_rng(seed)
+    cu = [0, 3, 3, 8, 9, 15]  # lengths 3, 0 (empty), 5, 1, 6
+    T, Hq, Hkv, d = cu[-1], 4, 2, 3
+    q = _rand((T, Hq, d), rng)
+    k = _rand((T, Hkv, d), rng)
+    v = _rand((T, Hkv, d + 1), rng)
+    for causal, window in [(False, -1), (True, -1), (False, 1), (True, 2)]:
+        O, L = orc.attention_varlen(q, k, v, cu, causal=causal, window=window, scale=0.6)
+        for s in range(len(cu) - 1):
+            a, e = cu[s], cu[s + 1]
+            if e == a:
+                continue
+            Ob, Lb = brute_attention(q[None, a:e], k[None, a:e], v[None, a:e], causal, window, 0.6)
+            _close(O[a:e], Ob[0], 1e-12, f"varlen O seq {s} {causal} {window}")
+            _close(L[:, a:e], Lb[0], 1e-12, f"varlen LSE seq {s} {causal} {window}")
+
+
 ALL_PINS = [
     pin_bruteforce, pin_torch_sdpa, pin_rows_sum_to_one, pin_constant_v, pin_single_key,
     pin_causal_first_row, pin_window_limits, pin_scale_zero, pin_hardmax_limit,
     pin_key_permutation, pin_gqa_mapping, pin_band_equals_dense, pin_golden,
-    pin_split_merge, pin_empty_rows,
+    pin_split_merge, pin_empty_rows, pin_varlen_bruteforce,
 ]

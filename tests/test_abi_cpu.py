@@ -123,3 +123,22 @@ def test_combine_validation(binding):
     assert lib.lse_tree_combine(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, None, 0) == UNSUPPORTED
     assert lib.lse_tree_combine(None, FAKE, FAKE, FAKE, FAKE, 4, 4, 64, None, 0) == INVALID
     assert lib.lse_tree_combine(None, None, None, None, None, 0, 4, 64, None, 0) == 0
+
+
+def test_varlen_validation(binding):
+    lib = binding.lib()
+
+    def call(S=2, T=100, maxlen=60, Hq=2, Hkv=2, d=64, ptr=FAKE, cu=FAKE, causal=0):
+        return lib.attn_fwd_varlen(ptr, ptr, ptr, ptr, ptr, cu, S, T, maxlen, Hq, Hkv, d, causal,
+                                   -1, 0.125, None, 0)
+    assert call(S=-1) == INVALID
+    assert call(S=4097) == UNSUPPORTED
+    assert "4096" in binding.last_error()
+    assert call(d=96) == UNSUPPORTED
+    assert call(Hq=3) == INVALID
+    assert call(cu=0) == INVALID
+    assert call(cu=FAKE + 2) == INVALID  # not 4-byte aligned
+    assert call(ptr=FAKE + 8) == INVALID
+    assert call(causal=3) == INVALID
+    assert call(S=0, ptr=0, cu=0) == 0
+    assert call(T=0, ptr=0, cu=0) == 0

@@ -30,6 +30,7 @@ MUTANTS = [
      "lo, hi = c * chunk, min((c + 1) * chunk - 1, n)"),
     ("partial_no_exp_o", "return m, e.sum(), e @ vv", "return m, e.sum(), vv.sum(axis=0)"),
     ("band_narrow", "c1 = min(N, r1 + window)", "c1 = min(N, r1 + window - 1)"),
+    ("varlen_slice_end", "O[a:e] = o_s[0]", "O[a:e] = o_s[0][::-1]"),
     ("empty_row_lse_zero", "lse = np.where(empty, NEG_INF, m_safe + np.log(l_safe))",
      "lse = np.where(empty, 0.0, m_safe + np.log(l_safe))"),
 ]
