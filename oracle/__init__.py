@@ -7,6 +7,7 @@ CUDA path.
 
 from .attention import (  # noqa: F401
     attention,
+    attention_backward,
     attention_band,
     attention_head,
     attention_rows,

@@ -141,6 +141,46 @@ def attention_varlen(q, k, v, cu_seqlens, causal: bool = False, window: int = -1
     return O, LSE
 
 
+def attention_backward(q, k, v, dO, causal: bool = False, window: int = -1,
+                       scale: float | None = None):
+    """Gradients of O = softmax(scale Q K^T + mask) V with respect to Q, K, V,
+    given dO = dLoss/dO, in float64.  For each (batch, head), with P the
+    attention weights of the forward definition:
+
+      dV   = P^T dO
+      dP   = dO V^T
+      dS   = P * (dP - rowsum(P * dP))        (the softmax Jacobian, row by row)
+      dQ   = scale dS K
+      dK   = scale dS^T Q
+
+    and rowsum(P * dP) = rowsum(dO * O).  Query heads of a group add their
+    dK, dV into the shared kv head.  q [B, N, Hq, d], k/v [B, N, Hkv, d],
+    dO [B, N, Hq, dv] -> dQ [B, N, Hq, d], dK [B, N, Hkv, d], dV [B, N, Hkv, dv].
+    """
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    vis = visible(Nq, Nk, causal, window)
+    dQ = np.zeros_like(q)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            _, _, P = attention_head(q[b, :, h], k[b, :, hk], v[b, :, hk], scale, vis,
+                                     return_p=True)
+            do = dO[b, :, h]
+            dV[b, :, hk] += P.T @ do
+            dP = do @ v[b, :, hk].T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dQ[b, :, h] = scale * (dS @ k[b, :, hk])
+            dK[b, :, hk] += scale * (dS.T @ q[b, :, h])
+    return dQ, dK, dV
+
+
 def attention_rows(q, k, v, b: int, h: int, rows, causal: bool = False, window: int = -1,
                    scale: float | None = None):
     """O and LSE for selected query rows of one (b, h): the same definition,

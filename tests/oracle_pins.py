@@ -345,9 +345,72 @@ def pin_varlen_bruteforce(orc, seed=13):
             _close(L[:, a:e], Lb[0], 1e-12, f"varlen LSE seq {s} {causal} {window}")
 
 
+def pin_backward_finite_differences(orc, seed=14):
+    """Gradients against central differences of the brute-force forward's
+    loss sum(dO * O): independent of the analytical backward formulas."""
+    rng = np.random.default_rng(seed)
+    for B, N, Hq, Hkv, d, causal, window, scale in [(1, 4, 2, 1, 3, True, -1, 0.8),
+                                                   (1, 5, 2, 2, 2, False, 1, 1.1)]:
+        q = _rand((B, N, Hq, d), rng)
+        k = _rand((B, N, Hkv, d), rng)
+        v = _rand((B, N, Hkv, d), rng)
+        dO = _rand((B, N, Hq, d), rng)
+        dQ, dK, dV = orc.attention_backward(q, k, v, dO, causal=causal, window=window,
+                                            scale=scale)
+
+        def loss(q_, k_, v_):
+            O, _ = brute_attention(q_, k_, v_, causal, window, scale)
+            return float((O * dO).sum())
+
+        eps = 1e-6
+        for arr, grad, which in ((q, dQ, 0), (k, dK, 1), (v, dV, 2)):
+            num = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                plus, minus = arr.copy(), arr.copy()
+                plus[idx] += eps
+                minus[idx] -= eps
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[which], args_m[which] = plus, minus
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            _close(grad, num, 1e-7, f"finite differences {which} {causal} {window}")
+
+
+def pin_backward_torch_autograd(orc, seed=15):
+    """Library cross-check: torch float64 autograd through a plain masked
+    softmax attention, grouped heads included."""
+    rng = np.random.default_rng(seed)
+    B, N, Hq, Hkv, d = 2, 9, 4, 2, 5
+    for causal, window in [(False, -1), (True, -1), (True, 3), (False, 2)]:
+        q = _rand((B, N, Hq, d), rng)
+        k = _rand((B, N, Hkv, d), rng)
+        v = _rand((B, N, Hkv, d), rng)
+        dO = _rand((B, N, Hq, d), rng)
+        tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+        G = Hq // Hkv
+        kk = tk.repeat_interleave(G, dim=2)
+        vv = tv.repeat_interleave(G, dim=2)
+        S = torch.einsum("bihd,bjhd->bhij", tq, kk) * 0.7
+        i = torch.arange(N)[:, None]
+        j = torch.arange(N)[None, :]
+        vis = torch.ones(N, N, dtype=torch.bool)
+        if causal:
+            vis &= j <= i
+        if window >= 0:
+            vis &= ((i - j) <= window) if causal else ((i - j).abs() <= window)
+        S = S.masked_fill(~vis, float("-inf"))
+        O = torch.einsum("bhij,bjhd->bihd", torch.softmax(S, dim=-1), vv)
+        (O * torch.tensor(dO)).sum().backward()
+        dQ, dK, dV = orc.attention_backward(q, k, v, dO, causal=causal, window=window, scale=0.7)
+        _close(dQ, tq.grad.numpy(), 1e-12, f"autograd dQ {causal} {window}")
+        _close(dK, tk.grad.numpy(), 1e-12, f"autograd dK {causal} {window}")
+        _close(dV, tv.grad.numpy(), 1e-12, f"autograd dV {causal} {window}")
+
+
 ALL_PINS = [
     pin_bruteforce, pin_torch_sdpa, pin_rows_sum_to_one, pin_constant_v, pin_single_key,
     pin_causal_first_row, pin_window_limits, pin_scale_zero, pin_hardmax_limit,
     pin_key_permutation, pin_gqa_mapping, pin_band_equals_dense, pin_golden,
-    pin_split_merge, pin_empty_rows, pin_varlen_bruteforce,
+    pin_split_merge, pin_empty_rows, pin_varlen_bruteforce, pin_backward_finite_differences,
+    pin_backward_torch_autograd,
 ]

@@ -31,6 +31,10 @@ MUTANTS = [
     ("partial_no_exp_o", "return m, e.sum(), e @ vv", "return m, e.sum(), vv.sum(axis=0)"),
     ("band_narrow", "c1 = min(N, r1 + window)", "c1 = min(N, r1 + window - 1)"),
     ("varlen_slice_end", "O[a:e] = o_s[0]", "O[a:e] = o_s[0][::-1]"),
+    ("bwd_drops_row_term", "dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))", "dS = P * dP"),
+    ("bwd_dk_no_scale", "dK[b, :, hk] += scale * (dS.T @ q[b, :, h])", "dK[b, :, hk] += dS.T @ q[b, :, h]"),
+    ("bwd_dv_untransposed", "dV[b, :, hk] += P.T @ do", "dV[b, :, hk] += P @ do"),
+    ("bwd_gqa_overwrites", "dK[b, :, hk] += scale", "dK[b, :, hk] = scale"),
     ("empty_row_lse_zero", "lse = np.where(empty, NEG_INF, m_safe + np.log(l_safe))",
      "lse = np.where(empty, 0.0, m_safe + np.log(l_safe))"),
 ]
