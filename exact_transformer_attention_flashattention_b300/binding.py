@@ -26,6 +26,9 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]),
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P,
                              _I]),
+    "attn_bwd_workspace_size": (_SZ, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I,
+                      _F, _P, _I]),
     "attn_decode_chunk": (_I, [_I, _I]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ,
@@ -142,6 +145,34 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, 
                                 S, T, int(max_seqlen), Hq, Hkv, d, int(bool(causal)), int(window),
                                 float(scale), _stream(stream), _odtype(out.dtype)))
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, window: int = -1,
+             scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd: q, dO [B,N,Hq,d], k/v [B,N,Hkv,d] bf16, o (bf16 or
+    f32) and lse [B,Hq,N] from the forward -> (dQ, dK, dV) bf16."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _need(t, name, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or dO.shape != q.shape:
+        raise ValueError("shapes of k, v or dO do not match q")
+    if o.shape != q.shape or not o.is_contiguous():
+        raise ValueError("o must be a contiguous tensor shaped like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(_lib.attn_bwd_workspace_size(B, Hq, N))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(_lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                         _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, Hq, Hkv, N, d,
+                         int(bool(causal)), int(window), float(scale), _stream(stream),
+                         _odtype(o.dtype)))
+    return dq, dk, dv
 
 
 def attn_decode_chunk(max_kv_len: int, num_splits: int) -> int:

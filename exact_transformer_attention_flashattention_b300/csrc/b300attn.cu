@@ -14,6 +14,7 @@
 #include <string>
 
 #include "b300attn.h"
+#include "backward.cuh"
 #include "decode.cuh"
 #include "prefill.cuh"
 
@@ -206,6 +207,40 @@ int launch_combine(const float* pm, const float* pl, const float* po, void* o, f
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return B300ATTN_OK;
+}
+
+template <int D>
+int launch_backward(const void* q, const void* k, const void* v, const BwdParams& p,
+                    cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  int rc;
+  if ((rc = make_map_4d(&tq, q, D, p.Hq, p.N, p.B, 64, 1, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "q")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tk, k, D, p.Hkv, p.N, p.B, 64, 1, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "k")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tv, v, D, p.Hkv, p.N, p.B, 64, 1, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "v")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tdo, p.dO, D, p.Hq, p.N, p.B, 64, 1, 128, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "dO")) != B300ATTN_OK)
+    return rc;
+  if ((rc = set_smem(bwd_dkdv_kernel<D>, DkdvSmem<D>::BYTES)) != B300ATTN_OK) return rc;
+  if ((rc = set_smem(bwd_dq_kernel<D>, DqSmem<D>::BYTES)) != B300ATTN_OK) return rc;
+  const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
+  bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  const long long ntile = (p.N + 127) / 128;
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * ntile),
+                       C::THREADS, DkdvSmem<D>::BYTES, stream>>>(tq, tk, tv, tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+  bwd_dq_kernel<D><<<static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * ntile),
+                     C::THREADS, DqSmem<D>::BYTES, stream>>>(tq, tk, tv, tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
   return B300ATTN_OK;
 }
 
@@ -411,6 +446,63 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                   : launch_prefill<64>(q, k, v, p, bound, stream);
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int N) {
+  if (B < 0 || Hq < 0 || N < 0) return 0;
+  return align256(static_cast<size_t>(B) * Hq * N * sizeof(float));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+             float scale, cudaStream_t stream, int o_dtype) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size (B=%d Hq=%d Hkv=%d N=%d d=%d)", B, Hq, Hkv,
+                N, d);
+  if (B == 0 || N == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (causal != 0 && causal != 1) return fail(B300ATTN_ERR_INVALID, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
+                static_cast<double>(scale));
+  const size_t need = attn_bwd_workspace_size(B, Hq, N);
+  if (!workspace || workspace_bytes < need)
+    return fail(B300ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : static_cast<size_t>(0));
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(B300ATTN_ERR_INVALID, "workspace must be 256-byte aligned");
+  const long long ntile = (static_cast<long long>(N) + 127) / 128;
+  if (static_cast<long long>(B) * Hq * ntile > 0x7fffffffLL ||
+      static_cast<long long>(B) * N * Hq / 8 + 1 > 0x7fffffffLL)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  BwdParams p;
+  p.o = o;
+  p.dO = static_cast<const __nv_bfloat16*>(dO);
+  p.lse = lse;
+  p.dvec = static_cast<float*>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.window = window < 0 ? -1 : window;
+  p.o_f32 = o_dtype == B300ATTN_F32;
+  p.scale = scale;
+  p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
+  return d == 128 ? launch_backward<128>(q, k, v, p, stream)
+                  : launch_backward<64>(q, k, v, p, stream);
+}
+
 int attn_decode_chunk(int max_kv_len, int num_splits) {
   if (max_kv_len < 1 || num_splits < 1)
     return fail(B300ATTN_ERR_INVALID, "max_kv_len=%d and num_splits=%d must be >= 1", max_kv_len,
@@ -494,16 +586,20 @@ int lse_tree_combine(const float* part_m, const float* part_l, const float* part
 int attn_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   const unsigned int zero = 0;
   if ((e = cudaMemcpyFromSymbol(&a, g_prefill_status, sizeof(a))) != cudaSuccess ||
-      (e = cudaMemcpyFromSymbol(&b, g_decode_status, sizeof(b))) != cudaSuccess)
+      (e = cudaMemcpyFromSymbol(&b, g_decode_status, sizeof(b))) != cudaSuccess ||
+      (e = cudaMemcpyFromSymbol(&c, g_bwd_status, sizeof(c))) != cudaSuccess)
     return cuda_fail(e, "reading the device status word");
-  if (a | b) {
+  if (a | b | c) {
     cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));
+    cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
     return fail(B300ATTN_ERR_TIMEOUT,
-                "a kernel gave up on a bounded wait (status bits prefill=0x%x decode=0x%x)", a, b);
+                "a kernel gave up on a bounded wait (status bits prefill=0x%x decode=0x%x "
+                "backward=0x%x)",
+                a, b, c);
   }
   return B300ATTN_OK;
 }

@@ -1,0 +1,582 @@
+// Attention backward on sm_103a: dQ, dK, dV of O = softmax(scale Q K^T + mask) V
+// recomputed tile by tile from the forward's saved LSE, so that, as in the
+// forward, no N x N matrix reaches global memory.
+//
+// With P_ij = 2^(scale log2e s_ij - log2e LSE_i) (the forward's softmax weights,
+// recovered exactly from the row's log-sum-exp), D_i = rowsum(dO_i * O_i):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three kernels:
+//   bwd_preprocess_kernel  D_i = rowsum(dO_i * O_i)                          (CUDA cores)
+//   bwd_dkdv_kernel        one CTA per (sequence, kv head, 128-key tile): K_j, V_j stay
+//                          in shared memory while Q_i, dO_i of every query head of the
+//                          group stream through a ring; S^T = K Q^T and dP^T = V dO^T in
+//                          tensor memory (keys on the lanes), P^T and dS^T written back as
+//                          bf16, then dV += P^T dO and dK += dS^T Q with P^T / dS^T read
+//                          from tensor memory.
+//   bwd_dq_kernel          one CTA per (sequence, query head, 128-query tile): Q_i, dO_i
+//                          stay; K_j, V_j stream; S = Q K^T, dP = dO V^T, dS back to
+//                          tensor memory, dQ += dS K.
+// Splitting dQ from dK/dV recomputes S and dP once more but needs no atomics and
+// gives a deterministic result.
+//
+// CTA layout of the two tile kernels (256 threads): warp 0 TMA producer, warp 1
+// MMA issuer (whole warp, one elected lane), warp 2 tensor-memory allocator,
+// warp 3 idle, warps 4-7 element-wise work (one tensor-memory lane = one row).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace b300 {
+
+__device__ unsigned int g_bwd_status;  // OR of kStatusBwd* bits (bounded waits that ran out)
+// which wait gave up (bits of g_bwd_status)
+constexpr unsigned kStatusBwdProducer = 32u, kStatusBwdMma = 64u, kStatusBwdCompute = 128u,
+                   kStatusBwdVec = 256u, kStatusBwdMmaP = 512u, kStatusBwdEpilogue = 1024u;
+
+struct BwdParams {
+  const void* o;          // forward output [B, N, Hq, d] (bf16 or f32: o_f32)
+  const __nv_bfloat16* dO;  // [B, N, Hq, d]
+  const float* lse;       // [B, Hq, N] natural log (forward)
+  float* dvec;            // [B, Hq, N] rowsum(dO * O)
+  void* dq;               // [B, N, Hq, d] bf16
+  void* dk;               // [B, N, Hkv, d] bf16
+  void* dv;               // [B, N, Hkv, d] bf16
+  int B, Hq, Hkv, N;
+  int causal, window, o_f32;
+  float scale, scale_log2;
+};
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+// One warp per (b, i, h) row; rows are numbered in the [B, N, Hq] order of O.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
+  if (row >= rows) return;
+  float acc = 0.f;
+  const __nv_bfloat16* dOr = p.dO + row * D;
+#pragma unroll
+  for (int e = lane; e < D; e += 32) {
+    const float o = p.o_f32 ? static_cast<const float*>(p.o)[row * D + e]
+                            : __bfloat162float(static_cast<const __nv_bfloat16*>(p.o)[row * D + e]);
+    acc = fmaf(__bfloat162float(dOr[e]), o, acc);
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) {
+    const int h = static_cast<int>(row % p.Hq);
+    const long long bi = row / p.Hq;
+    const int i = static_cast<int>(bi % p.N);
+    const int b = static_cast<int>(bi / p.N);
+    p.dvec[(static_cast<long long>(b) * p.Hq + h) * p.N + i] = acc;
+  }
+}
+
+// Query row q sees key k (same rule as the forward).
+__device__ __forceinline__ bool bwd_visible(int q, int k, int N, bool causal, int window) {
+  if (q >= N || k >= N) return false;
+  if (causal && k > q) return false;
+  if (window >= 0) {
+    if (q - k > window) return false;
+    if (!causal && k - q > window) return false;
+  }
+  return true;
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128;                  // rows of a Q, dO, K or V tile
+  static constexpr int DCH = D / 64;                // 128-byte swizzle atoms across d
+  static constexpr int TILE_BYTES = TILE * D * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int THREADS = 256;
+};
+
+// ---------------------------------------------------------------- dK, dV
+template <int D>
+struct DkdvSmem {
+  using C = BwdCfg<D>;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = C::TILE_BYTES;
+  static constexpr int RING_OFF = 2 * C::TILE_BYTES;              // stage: Q tile, dO tile
+  static constexpr int STAGE_BYTES = 2 * C::TILE_BYTES;
+  static constexpr int VEC_OFF = RING_OFF + C::STAGES * STAGE_BYTES;  // [2 slots][lse2, dvec][128] f32
+  static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * 128 * 4;
+  static constexpr int BYTES = BAR_OFF + 256 + 1024;  // barriers + TMEM address, alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  using L = DkdvSmem<D>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  float* vec = reinterpret_cast<float*>(smem + L::VEC_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* kv_full = bars;                // K_j, V_j landed
+  uint64_t* ring_full = bars + 1;          // [STAGES]
+  uint64_t* ring_empty = ring_full + STAGES;
+  uint64_t* s_full = ring_empty + STAGES;  // S^T and dP^T in tensor memory
+  uint64_t* p_ready = s_full + 1;          // P^T, dS^T written by the 128 compute threads
+  uint64_t* acc_done = p_ready + 1;        // every MMA done
+  uint64_t* vec_full = acc_done + 1;       // [2] per-query vectors staged (128 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int nkt = (N + 127) / 128;
+  const int jt = blockIdx.x % nkt;                 // key tile
+  const int hk = (blockIdx.x / nkt) % p.Hkv;
+  const int b = blockIdx.x / (nkt * p.Hkv);
+  const int G = p.Hq / p.Hkv;
+  const int c0 = jt * 128, c1 = min(c0 + 127, N - 1);
+  // query rows that see at least one key of this tile
+  int rlo = 0, rhi = N - 1;
+  if (p.causal) rlo = c0;
+  if (p.window >= 0) {
+    if (!p.causal) rlo = max(0, c0 - p.window);
+    rhi = min(N - 1, c1 + p.window);
+  }
+  const int ilo = rlo / 128, ihi = rhi / 128;
+  const int nq = ihi - ilo + 1;                   // query tiles per head
+  const int nsteps = G * nq;                      // (head, query tile) steps
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(&vec_full[0], 128);
+    mbar_init(&vec_full[1], 128);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // tensor memory: S^T [0,128)  dP^T [128,256)  dV [256,256+D)  dK [256+D,256+2D)
+  const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 256 + D;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      for (int cc = 0; cc < C::DCH; ++cc) {
+        tma_load_4d(smem + L::K_OFF + cc * (128 * 128), &tm_k, kv_full, cc * 64, hk, c0, b);
+        tma_load_4d(smem + L::V_OFF + cc * (128 * 128), &tm_v, kv_full, cc * 64, hk, c0, b);
+      }
+      int t = 0;
+      bool ok = true;
+      for (; t < nsteps && ok; ++t) {
+        const int s = t % STAGES;
+        if (t >= STAGES &&
+            !(ok = mbar_wait(&ring_empty[s], ((t / STAGES) - 1) & 1, &g_bwd_status,
+                             kStatusBwdProducer)))
+          break;
+        const int h = hk * G + t / nq;
+        const int r0 = (ilo + t % nq) * 128;
+        uint8_t* st = smem + L::RING_OFF + s * L::STAGE_BYTES;
+        mbar_arrive_expect_tx(&ring_full[s], 2 * C::TILE_BYTES);
+        for (int cc = 0; cc < C::DCH; ++cc) {
+          tma_load_4d(st + cc * (128 * 128), &tm_q, &ring_full[s], cc * 64, h, r0, b);
+          tma_load_4d(st + C::TILE_BYTES + cc * (128 * 128), &tm_do, &ring_full[s], cc * 64, h,
+                      r0, b);
+        }
+      }
+      for (int u = max(0, t - STAGES); u < t; ++u)
+        mbar_wait(&ring_full[u % STAGES], (u / STAGES) & 1, &g_bwd_status, kStatusBwdProducer);
+      mbar_wait(kv_full, 0, &g_bwd_status, kStatusBwdProducer);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    const uint32_t idS = idesc_bf16_f32(128, 128, false);
+    const uint32_t idO = idesc_bf16_f32(128, D, true);
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
+    const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + L::V_OFF), 16, 1024);
+    const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 16, 1024);
+    const uint64_t dRmn = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 128 * 128, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, kStatusBwdMma));
+    };
+    bool ok = wait(kv_full, 0);
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int s = t % STAGES;
+      if (!(ok = wait(&ring_full[s], (t / STAGES) & 1))) break;
+      tc_fence_after();
+      const uint64_t qK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+      const uint64_t doK = qK + static_cast<uint64_t>(C::TILE_BYTES >> 4);
+      // S^T = K Q^T and dP^T = V dO^T (keys on the lanes, queries on the columns)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+        umma_ss_warp(tS, dK0 + off, qK + off, idS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+        umma_ss_warp(tP, dV0 + off, doK + off, idS, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(s_full);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, &g_bwd_status,
+                                                   kStatusBwdMmaP)))) break;
+      tc_fence_after();
+      // dV += P^T dO and dK += dS^T Q: A from tensor memory (bf16 pairs), B the
+      // stage's dO / Q tile read MN-major, 16 queries per instruction
+      const uint64_t qMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+      const uint64_t doMN = qMN + static_cast<uint64_t>(C::TILE_BYTES >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_warp(tV, tS + kk * 8, doMN + ((kk * 16 * 128) >> 4), idO,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_warp(tK, tP + kk * 8, qMN + ((kk * 16 * 128) >> 4), idO,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&ring_empty[s]);
+    }
+    umma_commit_warp(acc_done);
+    wait(acc_done, 0);
+  } else if (warp >= 4) {
+    // ================================================================ element-wise
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row of this thread within the tile
+    const int key = c0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool causal = p.causal != 0;
+    bool ok = true;
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int h = hk * G + t / nq;
+      const int r0 = (ilo + t % nq) * 128;
+      // this step's per-query vectors: LSE (base 2) and D, staged in shared
+      // memory by the 128 threads (two slots; a slot is rewritten only after
+      // every thread has arrived for the step in between, i.e. read it)
+      float* lse2 = vec + (t & 1) * 256;
+      float* dvq = lse2 + 128;
+      {
+        const int q = r0 + r;
+        const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * N + q;
+        lse2[r] = (q < N) ? p.lse[vi] * kLog2e : 0.f;
+        dvq[r] = (q < N) ? p.dvec[vi] : 0.f;
+      }
+      mbar_arrive(&vec_full[t & 1]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&vec_full[t & 1], (t >> 1) & 1, &g_bwd_status,
+                                             kStatusBwdVec));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, &g_bwd_status, kStatusBwdCompute));
+      if (!ok) break;
+      tc_fence_after();
+      const bool full_tile = (r0 + 127 < N) && (c0 + 127 < N) &&
+                             (!causal || r0 >= c0 + 127) &&
+                             (p.window < 0 || (r0 + 127 - c0 <= p.window &&
+                                               (causal || c0 + 127 - r0 <= p.window)));
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t us[32], ud[32];
+        tmem_ld32(tS + lane_off + ch * 32, us);
+        tmem_ld32(tP + lane_off + ch * 32, ud);
+        tmem_wait_ld();
+        reg_fence(us);
+        reg_fence(ud);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int col = ch * 32 + 2 * e + h2;
+            const int q = r0 + col;
+            const bool vis = full_tile || bwd_visible(q, key, N, causal, p.window);
+            const float x = fmaf(__uint_as_float(us[2 * e + h2]), sl2, -lse2[col]);
+            const float pe = vis ? ex2_approx(x) : 0.f;
+            pv[h2] = pe;
+            dsv[h2] = pe * (__uint_as_float(ud[2 * e + h2]) - dvq[col]);
+          }
+          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(tS + lane_off + ch * 16, pk);
+        tmem_st16(tP + lane_off + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, &g_bwd_status, kStatusBwdEpilogue));
+    if (ok) {
+      tc_fence_after();
+      // every lane takes part in the (warp-collective) tensor-memory loads;
+      // only rows inside the sequence are stored
+      const size_t orow = (static_cast<size_t>(b) * N + min(key, N - 1)) * p.Hkv + hk;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tA = (which ? tK : tV) + lane_off;
+        const float mul = which ? p.scale : 1.f;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + orow * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          tmem_ld32_wait(tA + cc * 32, u);
+          if (key < N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * mul, __uint_as_float(u[8 * e + 1]) * mul);
+              w.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * mul, __uint_as_float(u[8 * e + 3]) * mul);
+              w.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * mul, __uint_as_float(u[8 * e + 5]) * mul);
+              w.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * mul, __uint_as_float(u[8 * e + 7]) * mul);
+              d4[e] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D>
+struct DqSmem {
+  using C = BwdCfg<D>;
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = C::TILE_BYTES;
+  static constexpr int RING_OFF = 2 * C::TILE_BYTES;  // stage: K tile, V tile
+  static constexpr int STAGE_BYTES = 2 * C::TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + C::STAGES * STAGE_BYTES;
+  static constexpr int BYTES = BAR_OFF + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using C = BwdCfg<D>;
+  using L = DqSmem<D>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;                 // Q_i, dO_i landed
+  uint64_t* ring_full = bars + 1;          // [STAGES]
+  uint64_t* ring_empty = ring_full + STAGES;
+  uint64_t* s_full = ring_empty + STAGES;
+  uint64_t* p_ready = s_full + 1;
+  uint64_t* acc_done = p_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int nqt = (N + 127) / 128;
+  const int it = blockIdx.x % nqt;  // query tile
+  const int h = (blockIdx.x / nqt) % p.Hq;
+  const int b = blockIdx.x / (nqt * p.Hq);
+  const int hk = h / (p.Hq / p.Hkv);
+  const int r0 = it * 128, r1 = min(r0 + 127, N - 1);
+  const int klo = (p.window >= 0) ? max(0, r0 - p.window) : 0;
+  const int khi = p.causal ? r1 : ((p.window >= 0) ? min(N - 1, r1 + p.window) : N - 1);
+  const int jlo = klo / 128, jhi = khi / 128;
+  const int nsteps = jhi - jlo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(acc_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // tensor memory: S [0,128)  dP [128,256)  dQ [256,256+D)
+  const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+      for (int cc = 0; cc < C::DCH; ++cc) {
+        tma_load_4d(smem + L::Q_OFF + cc * (128 * 128), &tm_q, q_full, cc * 64, h, r0, b);
+        tma_load_4d(smem + L::DO_OFF + cc * (128 * 128), &tm_do, q_full, cc * 64, h, r0, b);
+      }
+      int t = 0;
+      bool ok = true;
+      for (; t < nsteps && ok; ++t) {
+        const int s = t % STAGES;
+        if (t >= STAGES &&
+            !(ok = mbar_wait(&ring_empty[s], ((t / STAGES) - 1) & 1, &g_bwd_status,
+                             kStatusBwdProducer)))
+          break;
+        const int c0 = (jlo + t) * 128;
+        uint8_t* st = smem + L::RING_OFF + s * L::STAGE_BYTES;
+        mbar_arrive_expect_tx(&ring_full[s], 2 * C::TILE_BYTES);
+        for (int cc = 0; cc < C::DCH; ++cc) {
+          tma_load_4d(st + cc * (128 * 128), &tm_k, &ring_full[s], cc * 64, hk, c0, b);
+          tma_load_4d(st + C::TILE_BYTES + cc * (128 * 128), &tm_v, &ring_full[s], cc * 64, hk,
+                      c0, b);
+        }
+      }
+      for (int u = max(0, t - STAGES); u < t; ++u)
+        mbar_wait(&ring_full[u % STAGES], (u / STAGES) & 1, &g_bwd_status, kStatusBwdProducer);
+      mbar_wait(q_full, 0, &g_bwd_status, kStatusBwdProducer);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    const uint32_t idS = idesc_bf16_f32(128, 128, false);
+    const uint32_t idO = idesc_bf16_f32(128, D, true);
+    const uint64_t dQ0 = smem_desc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
+    const uint64_t dDO0 = smem_desc_sw128(smem_u32(smem + L::DO_OFF), 16, 1024);
+    const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 16, 1024);
+    const uint64_t dRmn = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 128 * 128, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, kStatusBwdMma));
+    };
+    bool ok = wait(q_full, 0);
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int s = t % STAGES;
+      if (!(ok = wait(&ring_full[s], (t / STAGES) & 1))) break;
+      tc_fence_after();
+      const uint64_t kK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+      const uint64_t vK = kK + static_cast<uint64_t>(C::TILE_BYTES >> 4);
+      // S = Q K^T and dP = dO V^T (queries on the lanes, keys on the columns)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+        umma_ss_warp(tS, dQ0 + off, kK + off, idS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+        umma_ss_warp(tP, dDO0 + off, vK + off, idS, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(s_full);
+      if (!(ok = wait(p_ready, t & 1))) break;
+      tc_fence_after();
+      // dQ += dS K: dS (bf16 pairs) from tensor memory, the stage's K tile read MN-major
+      const uint64_t kMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts_warp(tQ, tP + kk * 8, kMN + ((kk * 16 * 128) >> 4), idO,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&ring_empty[s]);
+    }
+    umma_commit_warp(acc_done);
+    wait(acc_done, 0);
+  } else if (warp >= 4) {
+    // ================================================================ element-wise
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row of this thread within the tile
+    const int row = r0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool causal = p.causal != 0;
+    const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * N + row;
+    const float lse2 = (row < N) ? p.lse[vi] * kLog2e : 0.f;
+    const float drow = (row < N) ? p.dvec[vi] : 0.f;
+    bool ok = true;
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int c0 = (jlo + t) * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, &g_bwd_status, kStatusBwdCompute));
+      if (!ok) break;
+      tc_fence_after();
+      const bool full_tile = (r0 + 127 < N) && (c0 + 127 < N) &&
+                             (!causal || r0 >= c0 + 127) &&
+                             (p.window < 0 || (r0 + 127 - c0 <= p.window &&
+                                               (causal || c0 + 127 - r0 <= p.window)));
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t us[32], ud[32];
+        tmem_ld32(tS + lane_off + ch * 32, us);
+        tmem_ld32(tP + lane_off + ch * 32, ud);
+        tmem_wait_ld();
+        reg_fence(us);
+        reg_fence(ud);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float dsv[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int key = c0 + ch * 32 + 2 * e + h2;
+            const bool vis = full_tile || bwd_visible(row, key, N, causal, p.window);
+            const float x = fmaf(__uint_as_float(us[2 * e + h2]), sl2, -lse2);
+            const float pe = vis ? ex2_approx(x) : 0.f;
+            dsv[h2] = pe * (__uint_as_float(ud[2 * e + h2]) - drow);
+          }
+          dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(tP + lane_off + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, &g_bwd_status, kStatusBwdEpilogue));
+    if (ok) {
+      tc_fence_after();
+      // every lane takes part in the (warp-collective) tensor-memory loads;
+      // only rows inside the sequence are stored
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dq) +
+                           ((static_cast<size_t>(b) * N + min(row, N - 1)) * p.Hq + h) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        tmem_ld32_wait(tQ + lane_off + cc * 32, u);
+        if (row >= N) continue;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+        const float mul = p.scale;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * mul, __uint_as_float(u[8 * e + 1]) * mul);
+          w.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * mul, __uint_as_float(u[8 * e + 3]) * mul);
+          w.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * mul, __uint_as_float(u[8 * e + 5]) * mul);
+          w.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * mul, __uint_as_float(u[8 * e + 7]) * mul);
+          d4[e] = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace b300

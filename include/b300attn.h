@@ -102,6 +102,39 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int o_dtype);
 
 /*
+ * attn_bwd_workspace_size -- bytes of workspace attn_bwd needs: the f32 row
+ * terms D = rowsum(dO * O) [B, Hq, N], 256-byte aligned.  0 on invalid input.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int N);
+
+/*
+ * attn_bwd -- gradients dQ, dK, dV of attn_fwd's O with respect to q, k, v,
+ * given dO, the forward's O and its LSE.
+ *
+ * The forward's softmax weights are recomputed tile by tile from the saved
+ * LSE (P = exp(scale q.k - LSE)), so that, as in the forward, the N x N
+ * matrices stay on chip; then dV = P^T dO, dP = dO V^T,
+ * dS = P * (dP - rowsum(dO * O)), dQ = scale dS K, dK = scale dS^T Q.  Query
+ * heads of a group add into their kv head's dK and dV.  (The pages stress
+ * faster training, "FlashAttention-3" article, "Benefits": the backward pass
+ * is what training runs besides the forward.)  Three launches: the row terms,
+ * dK/dV (one CTA per kv head and 128-key tile), dQ (one CTA per query head and
+ * 128-query tile); no atomics, so the result is deterministic.
+ *
+ *   q, o, dO   [B, N, Hq, d] (q, dO bf16; o bf16 or f32 as o_dtype says)
+ *   k, v       bf16 [B, N, Hkv, d]
+ *   lse        f32 [B, Hq, N] from attn_fwd with the same causal/window/scale
+ *   dq         bf16 [B, N, Hq, d];   dk, dv  bf16 [B, N, Hkv, d]
+ *   workspace  >= attn_bwd_workspace_size(B, Hq, N) bytes, 256-byte aligned
+ *   d in {64, 128}; other arguments as for attn_fwd.
+ * Errors: INVALID, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+             float scale, cudaStream_t stream, int o_dtype);
+
+/*
  * attn_decode_chunk -- keys per split used by attn_decode_splitkv:
  * ceil(max_kv_len / num_splits) rounded up to a multiple of 64.  Returns a
  * negative status on invalid arguments.

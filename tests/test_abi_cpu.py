@@ -142,3 +142,24 @@ def test_varlen_validation(binding):
     assert call(causal=3) == INVALID
     assert call(S=0, ptr=0, cu=0) == 0
     assert call(T=0, ptr=0, cu=0) == 0
+
+
+def test_backward_validation(binding):
+    lib = binding.lib()
+    assert binding.lib().attn_bwd_workspace_size(2, 4, 300) == (2 * 4 * 300 * 4 + 255) // 256 * 256
+
+    def call(B=1, Hq=2, Hkv=2, N=16, d=64, ptr=FAKE, ws=FAKE, ws_bytes=1 << 20, causal=0,
+             o_dtype=0):
+        return lib.attn_bwd(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ws, ws_bytes, B, Hq, Hkv,
+                            N, d, causal, -1, 0.125, None, o_dtype)
+    assert call(B=-1) == INVALID
+    assert call(Hq=3) == INVALID
+    assert call(d=80) == UNSUPPORTED
+    assert call(ptr=0) == INVALID
+    assert call(ptr=FAKE + 4) == INVALID
+    assert call(ws=0) == WORKSPACE
+    assert call(ws_bytes=8) == WORKSPACE
+    assert call(ws=FAKE + 16) == INVALID
+    assert call(causal=5) == INVALID
+    assert call(o_dtype=3) == INVALID
+    assert call(N=0, ptr=0, ws=0) == 0
