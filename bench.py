@@ -405,6 +405,38 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             "launches_per_step": 1, "timing": timing}
 
 
+def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
+    """The backward of the prefill workload (dQ, dK, dV from O, LSE and a random
+    dO).  Algorithmic work: five products of 2*d flops per unmasked pair (S, dP,
+    dV, dK, dQ), 2.5 times the forward's; the kernels recompute S and dP once
+    more for the separate dQ pass, which is not counted."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_flops
+    q, k, v, o, lse = prefill_case(w, "cuda")
+    fa.attn_fwd(q, k, v, causal=w.causal, window=w.window, scale=w.scale, out=o, lse=lse)
+    g = torch.Generator("cuda").manual_seed(w.seed + 100)
+    dO = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.attn_bwd_workspace_size(w.B, w.Hq, w.N), dtype=torch.uint8, device="cuda")
+    flops = 2.5 * prefill_flops(w.B, w.Hq, w.N, w.d, w.causal, w.window)
+
+    def step():
+        fa.attn_bwd(q, k, v, o, lse, dO, causal=w.causal, window=w.window, scale=w.scale,
+                    dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    ms = time_launches(step, steps, warmup, dist)
+    timing = dict(LAST_TIMING)
+    assert fa.device_status() == 0, fa.last_error()
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    rf = roofline(tflops, peak, "TFLOP/s", "tensor", None, flops, "FLOP")
+    rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
+            "launches_per_call": 3, "timing": timing,
+            "config": dict(workload_config(w), workload=w.name + "_backward")}
+
+
 def decode_case(w, dev):
     import torch
     from exact_transformer_attention_flashattention_b300 import binding as fa
@@ -711,6 +743,9 @@ def main():
                 continue
             extra[name] = bench_decode(WORKLOADS[name], max(3, min(args.steps, 50)),
                                        max(3, args.warmup), dist, peaks, peak_kind)
+        if w.name == "causal_prefill_4k":
+            extra["causal_prefill_4k_backward"] = bench_backward(
+                w, max(3, min(args.steps, 50)), max(3, args.warmup), dist, peaks, peak_kind)
         for name in ("window_encoder_8k", "causal_prefill_4k"):
             if name == w.name:
                 continue

@@ -147,6 +147,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, 
     return out, lse
 
 
+def attn_bwd_workspace_size(B: int, Hq: int, N: int) -> int:
+    return int(_lib.attn_bwd_workspace_size(B, Hq, N))
+
+
 def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, window: int = -1,
              scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Backward of attn_fwd: q, dO [B,N,Hq,d], k/v [B,N,Hkv,d] bf16, o (bf16 or
@@ -165,7 +169,7 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, window: int = -1,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = int(_lib.attn_bwd_workspace_size(B, Hq, N))
+    need = attn_bwd_workspace_size(B, Hq, N)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _check(_lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),

@@ -163,3 +163,14 @@ def test_backward_validation(binding):
     assert call(causal=5) == INVALID
     assert call(o_dtype=3) == INVALID
     assert call(N=0, ptr=0, ws=0) == 0
+
+
+def test_bench_and_tests_call_only_existing_binding_functions(binding):
+    """Every `fa.<name>` used by bench.py, the smoke check and the tests exists."""
+    import re
+    files = [os.path.join(ROOT, "bench.py"), os.path.join(ROOT, "__graft_entry__.py")]
+    files += [os.path.join(ROOT, "tests", f) for f in os.listdir(os.path.join(ROOT, "tests"))
+              if f.endswith(".py")]
+    for f in files:
+        for name in set(re.findall(r"\bfa\.(\w+)", open(f).read())):
+            assert hasattr(binding, name), f"{os.path.basename(f)} uses missing fa.{name}"
