@@ -35,6 +35,8 @@ SIGNATURES = {
                                  _P, _I]),
     "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                                          _P, _I]),
+    "attn_decode_splitkv_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                       _F, _I, _P, _SZ, _P, _I]),
     "attn_decode_partials": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "lse_tree_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I]),
     "attn_device_status": (_I, [_P]),
@@ -244,6 +246,40 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, kv_len, num_splits: int,
                                             _ptr(out), _ptr(lse), B, Hq, Hkv, Lmax, d,
                                             float(scale), int(num_splits), _stream(stream),
                                             _odtype(out.dtype)))
+    return out, lse
+
+
+def attn_decode_splitkv_paged(q, k_pages, v_pages, block_table, kv_len, num_splits: int,
+                              scale: float | None = None, out=None, lse=None, workspace=None,
+                              out_dtype=torch.bfloat16, stream=None):
+    """Split-KV decode over a paged cache.  q [B,Hq,d]; pages [P, page_size, Hkv, d]
+    bf16; block_table int32 [B, pages_per_seq]; kv_len int32 [B] -> (O, LSE)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(kv_len, "kv_len", torch.int32, 1)
+    B, Hq, d = q.shape
+    P, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if k_pages.shape != (P, page_size, Hkv, d) or v_pages.shape != k_pages.shape:
+        raise ValueError("page pool shapes do not match q")
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    pps = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace_size(B, Hq, num_splits, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(_lib.attn_decode_splitkv_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                          _ptr(block_table), _ptr(kv_len), _ptr(out), _ptr(lse),
+                                          B, Hq, Hkv, page_size, P, pps, d, float(scale),
+                                          int(num_splits), _ptr(workspace), workspace.numel(),
+                                          _stream(stream), _odtype(out.dtype)))
     return out, lse
 
 

@@ -166,10 +166,13 @@ int launch_decode(const void* k_cache, const void* v_cache, const DecodeParams& 
   using L = DecSmem<D, GT>;
   CUtensorMap tk, tv;
   int rc;
-  if ((rc = make_map_4d(&tk, k_cache, D, p.Hkv, p.Lmax, p.B, D, 1, kDecSub, 1,
+  // dense [B, Lmax, Hkv, D] or paged [num_pages, page_size, Hkv, D]
+  const uint64_t rows = p.block_table ? p.page_size : p.Lmax;
+  const uint64_t outer = p.block_table ? p.num_pages : p.B;
+  if ((rc = make_map_4d(&tk, k_cache, D, p.Hkv, rows, outer, D, 1, kDecSub, 1,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "k_cache")) != B300ATTN_OK)
     return rc;
-  if ((rc = make_map_4d(&tv, v_cache, D, p.Hkv, p.Lmax, p.B, D, 1, kDecSub, 1,
+  if ((rc = make_map_4d(&tv, v_cache, D, p.Hkv, rows, outer, D, 1, kDecSub, 1,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache")) != B300ATTN_OK)
     return rc;
   if ((rc = set_smem(decode_partial_kernel<D, GT>, L::BYTES)) != B300ATTN_OK) return rc;
@@ -301,6 +304,10 @@ int decode_setup(const void* q, const void* k_cache, const void* v_cache, const 
   p.S = num_splits;
   p.G = G;
   p.scale_log2 = scale * kLog2e;
+  p.block_table = nullptr;
+  p.page_size = 0;
+  p.pages_per_seq = 0;
+  p.num_pages = 0;
   return B300ATTN_OK;
 }
 
@@ -567,6 +574,46 @@ int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* 
   if (rc != B300ATTN_OK) return rc;
   return attn_decode_splitkv(q, k_cache, v_cache, kv_len, o, lse, B, Hq, Hkv, max_kv_len, d,
                              scale, num_splits, scratch, kNoAllocScratchBytes, stream, o_dtype);
+}
+
+int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* kv_len, void* o, float* lse,
+                              int B, int Hq, int Hkv, int page_size, int num_pages,
+                              int pages_per_seq, int d, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                              int o_dtype) {
+  if (page_size < 0 || num_pages < 0 || pages_per_seq < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative page geometry");
+  if (B > 0 && Hq > 0) {
+    if (page_size < kDecSub || page_size % kDecSub != 0)
+      return fail(B300ATTN_ERR_UNSUPPORTED, "page_size=%d must be a positive multiple of %d",
+                  page_size, kDecSub);
+    if (num_pages < 1 || pages_per_seq < 1)
+      return fail(B300ATTN_ERR_INVALID, "num_pages and pages_per_seq must be >= 1");
+    if (!block_table) return fail(B300ATTN_ERR_INVALID, "NULL block_table");
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+      return fail(B300ATTN_ERR_INVALID, "block_table must be 4-byte aligned");
+  }
+  const long long lmax = static_cast<long long>(pages_per_seq) * page_size;
+  if (lmax > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "sequence capacity too large");
+  DecodeParams p;
+  int GT = 1;
+  int rc = decode_setup(q, k_pages, v_pages, kv_len, B, Hq, Hkv, static_cast<int>(lmax), d,
+                        scale, num_splits, workspace, workspace_bytes, p, GT);
+  if (rc != B300ATTN_OK || p.B == 0) return rc;
+  if ((rc = check_common(d, o_dtype)) != B300ATTN_OK) return rc;
+  if (!o || !lse) return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(o) || !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  // the chunk is a multiple of the 64-key stage, and so is page_size: no
+  // stage straddles two pages
+  p.block_table = block_table;
+  p.page_size = page_size;
+  p.pages_per_seq = pages_per_seq;
+  p.num_pages = num_pages;
+  if ((rc = launch_partials(d, GT, k_pages, v_pages, p, stream)) != B300ATTN_OK) return rc;
+  return launch_combine(p.part_m, p.part_l, p.part_o, o, lse, B * Hq, num_splits, d,
+                        o_dtype == B300ATTN_F32, stream);
 }
 
 int lse_tree_combine(const float* part_m, const float* part_l, const float* part_o, void* o,

@@ -132,9 +132,13 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int nkt = (N + 127) / 128;
-  const int jt = blockIdx.x % nkt;                 // key tile
-  const int hk = (blockIdx.x / nkt) % p.Hkv;
-  const int b = blockIdx.x / (nkt * p.Hkv);
+  // Causal: the first key tiles are seen by the most query tiles, so the
+  // launch order is tile-major from the first key tile (heaviest CTAs first).
+  const int BH = p.B * p.Hkv;
+  const int jt = p.causal ? static_cast<int>(blockIdx.x / BH) : static_cast<int>(blockIdx.x % nkt);
+  const int bh = p.causal ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / nkt);
+  const int hk = bh % p.Hkv;
+  const int b = bh / p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int c0 = jt * 128, c1 = min(c0 + 127, N - 1);
   // query rows that see at least one key of this tile
@@ -392,9 +396,14 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int nqt = (N + 127) / 128;
-  const int it = blockIdx.x % nqt;  // query tile
-  const int h = (blockIdx.x / nqt) % p.Hq;
-  const int b = blockIdx.x / (nqt * p.Hq);
+  // Causal: the last query tiles see the most key tiles, so the launch order
+  // is tile-major from the last query tile (heaviest CTAs first).
+  const int BH = p.B * p.Hq;
+  const int it = p.causal ? nqt - 1 - static_cast<int>(blockIdx.x / BH)
+                          : static_cast<int>(blockIdx.x % nqt);
+  const int bh = p.causal ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / nqt);
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
   const int hk = h / (p.Hq / p.Hkv);
   const int r0 = it * 128, r1 = min(r0 + 127, N - 1);
   const int klo = (p.window >= 0) ? max(0, r0 - p.window) : 0;

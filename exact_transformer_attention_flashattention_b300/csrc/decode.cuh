@@ -39,6 +39,12 @@ struct DecodeParams {
   float* part_o;           // [B*Hq, S, D]
   int B, Hq, Hkv, Lmax, chunk, S, G;
   float scale_log2;
+  // Paged cache (block_table != NULL): K/V are [num_pages, page_size, Hkv, D]
+  // and logical key k of sequence b lives in physical page
+  // block_table[b * pages_per_seq + k / page_size], row k % page_size.
+  // page_size is a multiple of the 64-key stage, so a stage never straddles pages.
+  const int* block_table;
+  int page_size, pages_per_seq, num_pages;
 };
 
 template <int D>
@@ -142,8 +148,14 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
           break;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* dst = smem + s * C::STAGE_BYTES;
-        tma_load_4d(dst, &tm_k, &full[s], 0, hkv, key0 + issued * kDecSub, b);
-        tma_load_4d(dst + C::HALF_BYTES, &tm_v, &full[s], 0, hkv, key0 + issued * kDecSub, b);
+        const int key = key0 + issued * kDecSub;
+        int c2 = key, c3 = b;  // row and outer coordinate of the [.., rows, Hkv, D] view
+        if (p.block_table) {
+          c2 = key % p.page_size;
+          c3 = p.block_table[static_cast<size_t>(b) * p.pages_per_seq + key / p.page_size];
+        }
+        tma_load_4d(dst, &tm_k, &full[s], 0, hkv, c2, c3);
+        tma_load_4d(dst + C::HALF_BYTES, &tm_v, &full[s], 0, hkv, c2, c3);
       }
       for (int u = max(0, issued - STAGES); u < issued; ++u)
         mbar_wait(&full[u % STAGES], (u / STAGES) & 1, &g_decode_status, kStatusDecodeProducer);

@@ -211,6 +211,30 @@ int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* 
                                 cudaStream_t stream, int o_dtype);
 
 /*
+ * attn_decode_splitkv_paged -- attn_decode_splitkv over a paged KV cache, the
+ * layout inference servers keep for many sequences of changing length
+ * ("FlashAttention" learn page, "The future of FlashAttention": integration
+ * into inference servers).  Keys and values live in fixed-size pages of a
+ * shared pool; sequence b's logical key k is row k % page_size of physical
+ * page block_table[b * pages_per_seq + k / page_size].
+ *
+ *   k_pages, v_pages  bf16 [num_pages, page_size, Hkv, d]
+ *   block_table       int32 [B, pages_per_seq], device; entries for keys
+ *                     < kv_len[b] must lie in [0, num_pages) (others are not read;
+ *                     an out-of-range entry reads zeros, never out of bounds)
+ *   kv_len            int32 [B], device; clamped to [0, pages_per_seq * page_size]
+ *   page_size         a positive multiple of 64
+ *   other arguments, the split, the workspace and the errors as for
+ *   attn_decode_splitkv with max_kv_len = pages_per_seq * page_size.
+ */
+int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* kv_len, void* o, float* lse,
+                              int B, int Hq, int Hkv, int page_size, int num_pages,
+                              int pages_per_seq, int d, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                              int o_dtype);
+
+/*
  * attn_decode_partials -- the first half of attn_decode_splitkv on its own:
  * writes the per-split partial triples (m, l, o) of every query head into
  * `workspace` (layout as described for attn_decode_splitkv) and does not merge

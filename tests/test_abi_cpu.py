@@ -174,3 +174,21 @@ def test_bench_and_tests_call_only_existing_binding_functions(binding):
     for f in files:
         for name in set(re.findall(r"\bfa\.(\w+)", open(f).read())):
             assert hasattr(binding, name), f"{os.path.basename(f)} uses missing fa.{name}"
+
+
+def test_paged_decode_validation(binding):
+    lib = binding.lib()
+
+    def call(B=2, page=64, P=8, pps=4, ptr=FAKE, table=FAKE, ws=FAKE, S=2, d=128):
+        return lib.attn_decode_splitkv_paged(ptr, ptr, ptr, table, ptr, ptr, ptr, B, 4, 2, page,
+                                             P, pps, d, 0.1, S, ws, 1 << 30, None, 0)
+    assert call(page=100) == UNSUPPORTED
+    assert call(page=0) == UNSUPPORTED
+    assert call(P=0) == INVALID
+    assert call(pps=0) == INVALID
+    assert call(table=0) == INVALID
+    assert call(table=FAKE + 2) == INVALID
+    assert call(page=-64) == INVALID
+    assert call(ws=0) == WORKSPACE
+    assert call(d=96) == UNSUPPORTED
+    assert call(B=0, ptr=0, table=0, ws=0) == 0
