@@ -3,6 +3,8 @@
 TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
 benchmark's CPU-baseline leg, never by the library.  It shares no code with the
 CUDA path.
+
+``oracle.fp8`` adds the FP8 (e4m3) quantisation and FP8 attention.
 """
 
 from .attention import (  # noqa: F401
@@ -20,3 +22,4 @@ from .attention import (  # noqa: F401
     tree_combine,
     visible,
 )
+from . import fp8  # noqa: F401,E402

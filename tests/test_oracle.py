@@ -3,9 +3,15 @@
 import pytest
 
 import oracle
-from tests import oracle_pins
+import oracle.fp8
+from tests import oracle_pins, oracle_pins_fp8
 
 
 @pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
 def test_oracle_pin(pin):
     pin(oracle)
+
+
+@pytest.mark.parametrize("pin", oracle_pins_fp8.FP8_PINS, ids=lambda f: f.__name__)
+def test_oracle_fp8_pin(pin):
+    pin(oracle.fp8)

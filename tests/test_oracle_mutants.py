@@ -7,9 +7,10 @@ import types
 import numpy as np
 import pytest
 
-from tests import oracle_pins
+from tests import oracle_pins, oracle_pins_fp8
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "attention.py")
+SRC_FP8 = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "fp8.py")
 
 # (name, text in the oracle, planted replacement)
 MUTANTS = [
@@ -40,16 +41,39 @@ MUTANTS = [
 ]
 
 
-def _mutant_module(old, new):
-    src = open(SRC).read()
+# the same for the FP8 module (e4m3 rounding, scale exponents, tile layout,
+# the P-rounding error bound)
+MUTANTS_FP8 = [
+    ("round_half_away", "r = np.rint(a / step) * step", "r = np.floor(a / step + 0.5) * step"),
+    ("subnormal_step", "E4M3_SUBNORMAL_STEP = 2.0 ** -9", "E4M3_SUBNORMAL_STEP = 2.0 ** -10"),
+    ("no_saturation", "r = np.minimum(r, E4M3_MAX)", "r = r"),
+    ("exponent_tie_side", "e = np.where(f <= 0.875, 9 - x, 8 - x)",
+     "e = np.where(f < 0.875, 9 - x, 8 - x)"),
+    ("exponent_one_high", "e = np.where(f <= 0.875, 9 - x, 8 - x)",
+     "e = np.where(f <= 0.875, 10 - x, 9 - x)"),
+    ("dequant_wrong_sign", "deq[b, t * tile:(t + 1) * tile, h] = g * 2.0 ** -e",
+     "deq[b, t * tile:(t + 1) * tile, h] = g * 2.0 ** e"),
+    ("tile_overlaps_next", "blk = x[b, t * tile:(t + 1) * tile, h]",
+     "blk = x[b, t * tile:(t + 1) * tile + 1, h]"),
+    ("v_not_transposed_order", "codes[b, h, :, :N] = e4m3_encode(g).T",
+     "codes[b, h, :, :N] = e4m3_encode(g).T[::-1]"),
+    ("bound_no_floor", "eps = np.maximum(2.0 ** -4 * p, 2.0 ** -10) * (P > 0)",
+     "eps = 2.0 ** -4 * p * (P > 0)"),
+    ("bound_unnormalised", "l = 1.0 / pmax  # sum_j p_j = 1 / max_j P_j", "l = 1.0"),
+]
+
+
+def _mutant_module(old, new, src_path=SRC):
+    src = open(src_path).read()
     assert src.count(old) == 1, f"mutation anchor must occur exactly once: {old!r}"
     mod = types.ModuleType("oracle_mutant")
+    mod.__package__ = "oracle"  # relative imports resolve to the real oracle package
     exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
     return mod
 
 
-def _some_pin_fails(mod):
-    for pin in oracle_pins.ALL_PINS:
+def _some_pin_fails(mod, pins=None):
+    for pin in (oracle_pins.ALL_PINS if pins is None else pins):
         try:
             with np.errstate(all="ignore"):
                 pin(mod)
@@ -64,8 +88,18 @@ def test_planted_mistake_is_caught(name, old, new):
     assert caught is not None, f"no pin catches the planted mistake {name!r}"
 
 
+@pytest.mark.parametrize("name,old,new", MUTANTS_FP8, ids=[m[0] for m in MUTANTS_FP8])
+def test_planted_fp8_mistake_is_caught(name, old, new):
+    caught = _some_pin_fails(_mutant_module(old, new, SRC_FP8), oracle_pins_fp8.FP8_PINS)
+    assert caught is not None, f"no pin catches the planted mistake {name!r}"
+
+
 def test_unmutated_copy_passes():
     src = open(SRC).read()
     mod = types.ModuleType("oracle_copy")
     exec(compile(src, "oracle_copy", "exec"), mod.__dict__)
     assert _some_pin_fails(mod) is None
+    mod8 = types.ModuleType("oracle_fp8_copy")
+    mod8.__package__ = "oracle"
+    exec(compile(open(SRC_FP8).read(), "oracle_fp8_copy", "exec"), mod8.__dict__)
+    assert _some_pin_fails(mod8, oracle_pins_fp8.FP8_PINS) is None
