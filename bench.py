@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-extra] [--no-cpu-baseline] [--no-e2e]
+                    [--only backward|fp8]
 
 A "step" is one launch of the hot path on one batch of the workload: by default
 the causal prefill of B=4, Hq=Hkv=16, N=4096, d=128 (bf16 in, f32 accumulate,
@@ -51,6 +52,9 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="skip the decode/window sub-objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["backward", "fp8"], default=None,
+                    help="time one extra leg of a prefill workload alone and print its object "
+                         "(a small command for kernel profiles; not the benchmark line)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     return ap.parse_args()
@@ -66,15 +70,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha():
-    """Hash of the device-code sources (the .cuh files that define the
-    kernels); a stored ncu traffic figure is used only if it was taken from
-    the same device code."""
+# device-code files each profiled kernel is compiled from
+KERNEL_SOURCES = {
+    "prefill_kernel": ("prefill.cuh", "ptx.cuh"),
+    "decode_partial_kernel": ("decode.cuh", "ptx.cuh"),
+    "bwd_dkdv_kernel": ("backward.cuh", "ptx.cuh"),
+    "fp8_quantize_kernel": ("fp8.cuh", "ptx.cuh"),
+}
+
+
+def kernel_source_sha(kernel: str = "prefill_kernel"):
+    """Hash of the device code of `kernel` (the .cuh files it is compiled
+    from); a stored ncu traffic figure is used only if it was taken from the
+    same device code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, PKG, "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if not f.endswith(".cuh"):
-            continue
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -87,7 +98,7 @@ def stored_traffic(kernel: str, workload: str):
             rows = json.load(f)
     except (OSError, ValueError):
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kernel)
     for r in rows:
         if r.get("kernel") == kernel and r.get("workload") == workload and r.get("source_sha") == sha:
             return r.get("dram_bytes_per_launch")
@@ -437,6 +448,46 @@ def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
             "config": dict(workload_config(w), workload=w.name + "_backward")}
 
 
+def bench_fp8(w, steps, warmup, dist, peaks, peak_kind):
+    """FP8 (e4m3) prefill of the workload: the attention kernel alone on
+    operands quantised beforehand (as a model whose previous layer writes e4m3
+    would hand them over), and the quantisation of bf16 Q, K, V separately.
+    Roofline: the FP8 dense tensor peak, taken as the measured bf16 peak times
+    the nominal FP8/BF16 ratio (4.5 / 2.25 PFLOP/s)."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_flops
+    q, k, v, o, lse = prefill_case(w, "cuda")
+    qz = fa.attn_fp8_quantize(q, k, v)
+    ws = torch.empty(fa.attn_fp8_workspace_size(w.B, w.Hkv, w.N), dtype=torch.uint8,
+                     device="cuda")
+    flops = prefill_flops(w.B, w.Hq, w.N, w.d, w.causal, w.window)
+
+    def attn():
+        fa.attn_fwd_fp8(qz, causal=w.causal, window=w.window, scale=w.scale, out=o, lse=lse)
+
+    def quant():
+        fa.attn_fp8_quantize(q, k, v, out=qz, workspace=ws)
+
+    ms = time_launches(attn, steps, warmup, dist)
+    timing = dict(LAST_TIMING)
+    ms_q = time_launches(quant, steps, warmup, dist)
+    assert fa.device_status() == 0, fa.last_error()
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = round(peaks["bf16_tflops"] * 2.0, 1)
+    rf = roofline(tflops, peak, "TFLOP/s", "tensor",
+                  stored_traffic("prefill_kernel", w.name + "_fp8"), flops, "FLOP")
+    rf["peak_kind"] = f"{peak_kind} dense bf16 (burst) x 2, the nominal fp8/bf16 ratio"
+    q_bytes = (q.numel() + k.numel() + v.numel()) * 3  # 2 bytes read + 1 byte written each
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
+            "dtype": "e4m3 operands, f32 accumulate", "launches_per_call": 1, "timing": timing,
+            "quantize": {"ms_per_call": round(ms_q, 5), "launches_per_call": 2,
+                         "gbs": round(q_bytes / (ms_q * 1e-3) / 1e9, 1),
+                         "algorithmic_bytes": q_bytes},
+            "tflops_including_quantize": round(flops / ((ms + ms_q) * 1e-3) / 1e12, 2),
+            "config": dict(workload_config(w), workload=w.name + "_fp8")}
+
+
 def decode_case(w, dev):
     import torch
     from exact_transformer_attention_flashattention_b300 import binding as fa
@@ -707,6 +758,13 @@ def main():
     torch.cuda.set_device(dist.local)
     from exact_transformer_attention_flashattention_b300 import binding  # noqa: F401 (loads .so)
     peaks, peak_kind = load_peaks()
+    if args.only:
+        leg = bench_backward if args.only == "backward" else bench_fp8
+        res = leg(w, args.steps, args.warmup, dist, peaks, peak_kind)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        dist.close()
+        return
     clocks = ClockSampler(torch.cuda.current_device())
     if w.kind == "prefill":
         main_res = bench_prefill(w, args.steps, args.warmup, dist, peaks, peak_kind, clocks)
@@ -746,6 +804,8 @@ def main():
         if w.name == "causal_prefill_4k":
             extra["causal_prefill_4k_backward"] = bench_backward(
                 w, max(3, min(args.steps, 50)), max(3, args.warmup), dist, peaks, peak_kind)
+            extra["causal_prefill_4k_fp8"] = bench_fp8(
+                w, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks, peak_kind)
         for name in ("window_encoder_8k", "causal_prefill_4k"):
             if name == w.name:
                 continue

@@ -27,6 +27,12 @@ SIGNATURES = {
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P,
                              _I]),
     "attn_bwd_workspace_size": (_SZ, [_I, _I, _I]),
+    "attn_fp8_padded_len": (_I, [_I]),
+    "attn_fp8_workspace_size": (_SZ, [_I, _I, _I]),
+    "attn_fp8_quantize": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ,
+                               _P]),
+    "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P,
+                          _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I,
                       _F, _P, _I]),
     "attn_decode_chunk": (_I, [_I, _I]),
@@ -179,6 +185,73 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, window: int = -1,
                          int(bool(causal)), int(window), float(scale), _stream(stream),
                          _odtype(o.dtype)))
     return dq, dk, dv
+
+
+def attn_fp8_padded_len(N: int) -> int:
+    return int(_lib.attn_fp8_padded_len(N))
+
+
+def attn_fp8_workspace_size(B: int, Hkv: int, N: int) -> int:
+    return int(_lib.attn_fp8_workspace_size(B, Hkv, N))
+
+
+def attn_fp8_quantize(q, k, v, out=None, workspace=None, stream=None):
+    """bf16 q [B,N,Hq,d], k/v [B,N,Hkv,d] -> dict of e4m3 codes (uint8 tensors)
+    and int32 exponents: q8 [B,N,Hq,d], k8 [B,N,Hkv,d], v8t [B,Hkv,d,Np],
+    q_exp [B,Hq,nt], k_exp [B,Hkv,nt], v_exp [B,Hkv] (nt = ceil(N/128)).
+    ``out`` may hold preallocated tensors under the same names."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 4)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    nt, Np = (N + 127) // 128, attn_fp8_padded_len(N)
+    dev = q.device
+    shapes = {"q8": ((B, N, Hq, d), torch.uint8), "k8": ((B, N, Hkv, d), torch.uint8),
+              "v8t": ((B, Hkv, d, Np), torch.uint8), "q_exp": ((B, Hq, nt), torch.int32),
+              "k_exp": ((B, Hkv, nt), torch.int32), "v_exp": ((B, Hkv), torch.int32)}
+    out = dict(out or {})
+    for name, (shape, dt) in shapes.items():
+        if name not in out:
+            out[name] = torch.empty(shape, dtype=dt, device=dev)
+        t = out[name]
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {shape}")
+    need = attn_fp8_workspace_size(B, Hkv, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(_lib.attn_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), _ptr(out["q8"]), _ptr(out["k8"]),
+                                  _ptr(out["v8t"]), _ptr(out["q_exp"]), _ptr(out["k_exp"]),
+                                  _ptr(out["v_exp"]), B, Hq, Hkv, N, d, _ptr(workspace),
+                                  workspace.numel(), _stream(stream)))
+    return out
+
+
+def attn_fwd_fp8(qz, causal: bool = False, window: int = -1, scale: float | None = None,
+                 out=None, lse=None, out_dtype=torch.bfloat16, stream=None):
+    """Prefill attention on the e4m3 operands of ``attn_fp8_quantize`` (the dict
+    it returns) -> (O [B,N,Hq,d], LSE [B,Hq,N])."""
+    q8, k8, v8t = qz["q8"], qz["k8"], qz["v8t"]
+    for name, t, nd in (("q8", q8, 4), ("k8", k8, 4), ("v8t", v8t, 4)):
+        _need(t, name, torch.uint8, nd)
+    for name in ("q_exp", "k_exp", "v_exp"):
+        _need(qz[name], name, torch.int32, 3 if name != "v_exp" else 2)
+    B, N, Hq, d = q8.shape
+    Hkv = k8.shape[2]
+    if k8.shape != (B, N, Hkv, d) or v8t.shape != (B, Hkv, d, attn_fp8_padded_len(N)):
+        raise ValueError("k8 / v8t shapes do not match q8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, Hq, d), dtype=out_dtype, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device)
+    _check(_lib.attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(qz["q_exp"]), _ptr(qz["k_exp"]),
+                             _ptr(qz["v_exp"]), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
+                             int(bool(causal)), int(window), float(scale), _stream(stream),
+                             _odtype(out.dtype)))
+    return out, lse
 
 
 def attn_decode_chunk(max_kv_len: int, num_splits: int) -> int:

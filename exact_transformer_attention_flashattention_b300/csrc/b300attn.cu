@@ -16,6 +16,7 @@
 #include "b300attn.h"
 #include "backward.cuh"
 #include "decode.cuh"
+#include "fp8.cuh"
 #include "prefill.cuh"
 
 using namespace b300;
@@ -73,17 +74,20 @@ int make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   return B300ATTN_OK;
 }
 
-// 3-D bf16 tensor map over a row-major [d2][d1][d0] array (d0 contiguous).
+// 3-D tensor map over a row-major [d2][d1][d0] array (d0 contiguous) of bf16
+// elements, or of bytes when `bytes` is set (e4m3 codes).
 int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                 uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swizzle,
-                const char* name) {
+                const char* name, bool bytes = false) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const uint64_t es = bytes ? 1 : 2;
   const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
   const cuuint32_t box[3] = {b0, b1, b2};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  const CUresult r = fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -159,6 +163,36 @@ int launch_prefill(const void* q, const void* k, const void* v, const PrefillPar
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return B300ATTN_OK;
 }
+
+// FP8 prefill (d = 128, dense): q8 [B*N, Hq, 128] and k8 [B*N, Hkv, 128]
+// e4m3 seen as [rows, heads, d] with one 128-byte box per row; v8t
+// [B*Hkv, 128, Np] with boxes of 128 keys x all of d.
+int launch_prefill_fp8(const void* q8, const void* k8, const void* v8t, int Np,
+                       const PrefillParams& p, cudaStream_t stream) {
+  using C = PrefillCfg<128, true>;
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map_3d(&tq, q8, 128, p.Hq, p.total_rows, 128, 1, C::BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q8", true)) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_3d(&tk, k8, 128, p.Hkv, p.total_rows, 128, 1, C::BN,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k8", true)) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_3d(&tv, v8t, Np, 128, static_cast<uint64_t>(p.B) * p.Hkv, C::BN, 128, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v8t", true)) != B300ATTN_OK)
+    return rc;
+  auto kernel = prefill_kernel<128, false, true>;
+  if ((rc = set_smem(kernel, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != B300ATTN_OK) return rc;
+  const int grid = std::min(p.n_items, sms);
+  kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 prefill launch");
+  return B300ATTN_OK;
+}
+
+int fp8_padded_len(int N) { return (N + 15) / 16 * 16; }
 
 template <int D, int GT>
 int launch_decode(const void* k_cache, const void* v_cache, const DecodeParams& p,
@@ -383,7 +417,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (static_cast<long long>(B) * N > 0x7fffffffLL)
     return fail(B300ATTN_ERR_UNSUPPORTED, "B*N=%lld rows exceed 2^31-1",
                 static_cast<long long>(B) * N);
-  PrefillParams p;
+  PrefillParams p{};
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = nullptr;
@@ -430,7 +464,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   if (!std::isfinite(scale) || scale < 0.f)
     return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
                 static_cast<double>(scale));
-  PrefillParams p;
+  PrefillParams p{};
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu_seqlens;
@@ -451,6 +485,119 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   if (bound > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
   return d == 128 ? launch_prefill<128>(q, k, v, p, bound, stream)
                   : launch_prefill<64>(q, k, v, p, bound, stream);
+}
+
+size_t attn_fp8_workspace_size(int B, int Hkv, int N) {
+  if (B <= 0 || Hkv <= 0 || N <= 0) return 256;
+  return align256(static_cast<size_t>(B) * Hkv * ((N + 127) / 128) * sizeof(float));
+}
+
+int attn_fp8_padded_len(int N) { return N <= 0 ? 0 : fp8_padded_len(N); }
+
+int attn_fp8_quantize(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8t,
+                      int* q_exp, int* k_exp, int* v_exp, int B, int Hq, int Hkv, int N, int d,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size (B=%d Hq=%d Hkv=%d N=%d d=%d)", B, Hq, Hkv,
+                N, d);
+  if (B == 0 || N == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (d != 128)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "FP8 path: head dimension d=%d is not supported (128)",
+                d);
+  if (!q || !k || !v || !q8 || !k8 || !v8t || !q_exp || !k_exp || !v_exp)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(v8t))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (static_cast<long long>(B) * N > 0x7fffffffLL)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "B*N=%lld rows exceed 2^31-1",
+                static_cast<long long>(B) * N);
+  const size_t need = attn_fp8_workspace_size(B, Hkv, N);
+  if (!workspace || workspace_bytes < need)
+    return fail(B300ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : static_cast<size_t>(0));
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(B300ATTN_ERR_INVALID, "workspace must be 256-byte aligned");
+  Fp8QuantParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.q8 = static_cast<uint8_t*>(q8);
+  p.k8 = static_cast<uint8_t*>(k8);
+  p.v8t = static_cast<uint8_t*>(v8t);
+  p.q_exp = q_exp;
+  p.k_exp = k_exp;
+  p.v_exp = v_exp;
+  p.v_tile_amax = static_cast<float*>(workspace);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.Np = fp8_padded_len(N);
+  p.nt = (N + 127) / 128;
+  if (p.nt > 65535 || Hkv > 65535 || B > 65535)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "grid too large");
+  fp8_vamax_kernel<128><<<dim3(p.nt, Hkv, B), kFp8QuantThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 V maximum launch");
+  const long long jobs = static_cast<long long>(B) * p.nt * (Hq + 2LL * Hkv);
+  if (jobs > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many tiles");
+  fp8_quantize_kernel<128><<<static_cast<unsigned>(jobs), kFp8QuantThreads, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "FP8 quantize launch");
+  return B300ATTN_OK;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const int* q_exp,
+                 const int* k_exp, const int* v_exp, void* o, float* lse, int B, int Hq, int Hkv,
+                 int N, int d, int causal, int window, float scale, cudaStream_t stream,
+                 int o_dtype) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 0 || d < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size (B=%d Hq=%d Hkv=%d N=%d d=%d)", B, Hq, Hkv,
+                N, d);
+  if (B == 0 || N == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (d != 128)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "FP8 path: head dimension d=%d is not supported (128)",
+                d);
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (!q8 || !k8 || !v8t || !q_exp || !k_exp || !v_exp || !o || !lse)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (causal != 0 && causal != 1) return fail(B300ATTN_ERR_INVALID, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
+                static_cast<double>(scale));
+  if (static_cast<long long>(B) * N > 0x7fffffffLL)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "B*N=%lld rows exceed 2^31-1",
+                static_cast<long long>(B) * N);
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = nullptr;
+  p.num_seqs = B;
+  p.total_rows = B * N;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.window = window < 0 ? -1 : window;
+  p.o_f32 = o_dtype == B300ATTN_F32;
+  p.nqb = (N + 255) / 256;
+  p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
+  p.q_exp = q_exp;
+  p.k_exp = k_exp;
+  p.v_exp = v_exp;
+  p.nt = (N + 127) / 128;
+  const long long items = static_cast<long long>(p.nqb) * Hq * B;
+  if (items > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
+  p.n_items = static_cast<int>(items);
+  return launch_prefill_fp8(q8, k8, v8t, fp8_padded_len(N), p, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int N) {

@@ -66,21 +66,31 @@ struct PrefillParams {
   int nqb;           // dense: number of 256-row query blocks per sequence
   int n_items;       // dense: nqb * B * Hq (variable length: counted on the device)
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+  // FP8 (dense layout only): a stored code c stands for c * 2^-e, with e the
+  // exponent of its 128-row tile (Q, K) or of its head (V)
+  const int* q_exp;  // [B, Hq, nt]
+  const int* k_exp;  // [B, Hkv, nt]
+  const int* v_exp;  // [B, Hkv]
+  int nt;            // 128-row tiles per sequence
 };
 
-template <int D>
+template <int D, bool FP8 = false>
 struct PrefillCfg {
+  static constexpr int EB = FP8 ? 1 : 2;  // bytes per element of Q, K, V
   static constexpr int BM = 128;  // query rows per Q tile (one softmax warpgroup)
   static constexpr int BN = 128;  // keys per K/V tile
-  static constexpr int DCH = D / 64;  // 128-byte swizzle atoms across d
-  static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (bf16)
+  static constexpr int DCH = D * EB / 128;  // 128-byte swizzle atoms across d
+  static constexpr int TILE_BYTES = BM * D * EB;  // one Q, K or V tile
   // Q is double-buffered (the next item's Q loads while the current item
-  // runs) when shared memory allows: at d=64 always; at d=128 the K/V ring
-  // would have to shrink to three stages, so one Q buffer is kept there.
-  static constexpr int QBUF = (D == 128) ? 1 : 2;
-  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  // runs) when shared memory allows: at d=64 and in FP8 always; at d=128 in
+  // bf16 the K/V ring would have to shrink to three stages, so one Q buffer
+  // is kept there.
+  static constexpr int QBUF = (D == 128 && !FP8) ? 1 : 2;
+  static constexpr int STAGES = FP8 ? 6 : ((D == 128) ? 4 : 8);
   static constexpr int RING_OFF = QBUF * 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
+  // FP8: the e4m3 P tile of each Q tile (128 rows x 128 keys, 128-byte swizzle)
+  static constexpr int P_OFF = RING_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = P_OFF + (FP8 ? 2 * BM * BN : 0);
   // + barriers and the TMEM address (512 B), the variable-length item table
   // (kMaxVarlenSeqs + 1 ints), alignment slack
   static constexpr int TABLE_OFF = BAR_OFF + 512;
@@ -173,11 +183,20 @@ __device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p,
 
 // VARLEN selects the layout at compile time, so that the dense launch carries
 // none of the variable-length bookkeeping.
-template <int D, bool VARLEN>
+//
+// FP8 selects e4m3 operands (dense layout, d = 128): Q and K tiles as in bf16
+// but one byte per element, V stored transposed ([B, Hkv, d, Np], so that the
+// PV product reads it K-major), tcgen05 kind::f8f6f4 with 32 elements of K
+// per instruction.  The softmax multiplies the raw scores by
+// scale * 2^-(e_Q + e_K) of the tile pair, writes P rounded to e4m3 into a
+// swizzled shared-memory tile (the A operand of PV), and the epilogue divides
+// by l and by 2^e_V.  The lazy rescale keeps P <= 2^8 < 448, inside e4m3.
+template <int D, bool VARLEN, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using C = PrefillCfg<D>;
+  static_assert(!FP8 || (D == 128 && !VARLEN), "FP8: dense layout, d = 128");
+  using C = PrefillCfg<D, FP8>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -299,7 +318,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(qf, C::TILE_BYTES);
           for (int cc = 0; cc < C::DCH; ++cc)
             tma_load_3d(sQ + (qs * 2 + i) * C::TILE_BYTES + cc * (C::BM * 128), &tm_q, qf,
-                        cc * 64, it.h, it.base + it.qb * 256 + i * 128);
+                        cc * (128 / C::EB), it.h, it.base + it.qb * 256 + i * 128);
         }
         const int nloads = 2 * (it.J1 - it.J0 + 1);  // K_j, V_j alternate in the ring
         for (int u = 0; u < nloads && ok; ++u, ++issued) {
@@ -310,10 +329,19 @@ __global__ void __launch_bounds__(384, 1)
             break;
           mbar_arrive_expect_tx(&kv_full[s], C::TILE_BYTES);
           const int j = it.J0 + u / 2;
-          const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
-          for (int cc = 0; cc < C::DCH; ++cc)
-            tma_load_3d(sRing + s * C::TILE_BYTES + cc * (BN * 128), tm, &kv_full[s], cc * 64,
-                        it.hk, it.base + j * BN);
+          if constexpr (FP8) {
+            if (u & 1)  // V^T tile: keys [j*BN, j*BN + BN) x all of d, of plane (b, hk)
+              tma_load_3d(sRing + s * C::TILE_BYTES, &tm_v, &kv_full[s], j * BN, 0,
+                          it.b * p.Hkv + it.hk);
+            else
+              tma_load_3d(sRing + s * C::TILE_BYTES, &tm_k, &kv_full[s], 0, it.hk,
+                          it.base + j * BN);
+          } else {
+            const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
+            for (int cc = 0; cc < C::DCH; ++cc)
+              tma_load_3d(sRing + s * C::TILE_BYTES + cc * (BN * 128), tm, &kv_full[s], cc * 64,
+                          it.hk, it.base + j * BN);
+          }
         }
       }
       // Every issued copy has landed before the CTA may exit (a no-op wait on
@@ -329,37 +357,52 @@ __global__ void __launch_bounds__(384, 1)
     // ================================================================ MMA issuer
     // The whole warp runs this loop (waits included); one elected lane issues
     // each tcgen05 instruction.  Descriptors are a base plus constant offsets.
-    const uint32_t idS = idesc_bf16_f32(128, BN, false);
-    const uint32_t idO = idesc_bf16_f32(128, D, true);
+    const uint32_t idS = FP8 ? idesc_e4m3_f32(128, BN) : idesc_bf16_f32(128, BN, false);
+    const uint32_t idO = FP8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
     const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(smem_u32(sRing), 16, 1024);
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sRing), BN * 128, 1024);
+    const uint64_t dp0 = smem_desc_sw128(smem_u32(smem + C::P_OFF), 16, 1024);
     uint32_t pcnt[2] = {0u, 0u};  // p_full phases consumed, per Q tile
     uint32_t ocnt[2] = {0u, 0u};  // items in which Q tile i was active
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_prefill_status, kStatusMma));
     };
 
-    // S_i = Q_i K^T: K-major operands, 16 elements of d per instruction.
+    // S_i = Q_i K^T: K-major operands, 32 bytes of d per instruction (16
+    // bf16 or 32 e4m3 elements).
     int qs = 0;  // Q buffer of the current item
     auto issue_S = [&](int i, int stage) {
       const uint64_t a0 = dq0 + static_cast<uint64_t>(((qs * 2 + i) * C::TILE_BYTES) >> 4);
       const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < D * C::EB / 32; ++kk) {
         const uint32_t off = ((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tmem + i * 128, a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
+        if constexpr (FP8)
+          umma_ss_f8_warp(tmem + i * 128, a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
+        else
+          umma_ss_warp(tmem + i * 128, a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
       }
       umma_commit_warp(&s_full[i]);
     };
-    // O_i += P_i V: P (bf16 pairs) from tensor memory, V MN-major in shared
-    // memory, 16 keys per instruction.
+    // O_i += P_i V.  bf16: P (bf16 pairs) from tensor memory, V MN-major in
+    // shared memory, 16 keys per instruction.  FP8: P (e4m3) and V^T both
+    // K-major in shared memory, 32 keys per instruction.
     auto issue_PV = [&](int i, int stage, bool accumulate) {
-      const uint64_t b0 = dv0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
+      if constexpr (FP8) {
+        const uint64_t a0 = dp0 + static_cast<uint64_t>((i * C::BM * BN) >> 4);
+        const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        umma_ts_warp(tmem + 256 + i * D, tmem + i * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4), idO,
-                     (accumulate || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 32; ++kk)
+          umma_ss_f8_warp(tmem + 256 + i * D, a0 + ((kk * 32) >> 4), b0 + ((kk * 32) >> 4), idO,
+                          (accumulate || kk > 0) ? 1u : 0u);
+      } else {
+        const uint64_t b0 = dv0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts_warp(tmem + 256 + i * D, tmem + i * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
+                       idO, (accumulate || kk > 0) ? 1u : 0u);
+      }
     };
 
     bool ok = true;
@@ -455,7 +498,22 @@ __global__ void __launch_bounds__(384, 1)
       const int row = r0 + r;
       float m_ref = -INFINITY;  // base-2 running maximum actually used for P
       float l = 0.f;
+      // FP8: per-tile score multiplier scale * log2(e) * 2^-(e_Q + e_K); the
+      // exponent of the next key tile is loaded one tile ahead
+      const int* kexp = nullptr;
+      float qsc = 1.f;
+      int ek_next = 0;
+      if constexpr (FP8) {
+        qsc = pow2i(-p.q_exp[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.nt + it.qb * 2 + i]);
+        kexp = p.k_exp + (static_cast<size_t>(it.b) * p.Hkv + it.hk) * p.nt;
+        ek_next = kexp[jlo];
+      }
       for (int j = jlo; j <= jhi; ++j, ++scnt) {
+        float c = sl2;
+        if constexpr (FP8) {
+          c = fmaxf(sl2 * qsc * pow2i(-ek_next), 1e-30f);
+          if (j < jhi) ek_next = kexp[j + 1];
+        }
         ok = mbar_wait(&s_full[i], scnt & 1, &g_prefill_status, kStatusSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -506,7 +564,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int t = 0; t < 4; ++t) mc[t] = fmax3(mc[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
         const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-        const float m_new = fmaxf(m_ref, mx * sl2);
+        const float m_new = fmaxf(m_ref, mx * c);
         const bool resc = m_new > m_ref + kRescaleThreshold;
         float alpha = 1.f;
         if (resc) {
@@ -516,24 +574,47 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
         // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
-        // in four packed partial sums, bf16 pairs into tensor memory
-        const float2 sl2x2 = make_float2(sl2, sl2);
+        // in four packed partial sums; bf16 pairs into tensor memory, or e4m3
+        // quadruples into the swizzled shared-memory P tile
+        const float2 sl2x2 = make_float2(c, c);
         const float2 nmu2 = make_float2(neg_mu, neg_mu);
         float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t pk[16];
+          float pv[32];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 x =
                 ffma2(make_float2(s[q * 32 + 2 * e], s[q * 32 + 2 * e + 1]), sl2x2, nmu2);
             const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             lacc[e & 3] = fadd2(lacc[e & 3], pe);
-            pk[e] = pack_bf16x2(pe.x, pe.y);
+            if constexpr (FP8) {
+              pv[2 * e] = pe.x;
+              pv[2 * e + 1] = pe.y;
+            } else {
+              pk[e] = pack_bf16x2(pe.x, pe.y);
+            }
           }
-          tmem_st16(tS + q * 16, pk);
+          if constexpr (FP8) {
+            // keys 32q .. 32q+31 are 16-byte chunks 2q and 2q+1 of this row;
+            // chunk k of row r sits at position k ^ (r mod 8) (128-byte swizzle)
+            const uint32_t prow = smem_u32(smem + C::P_OFF) + i * (C::BM * BN) + (r >> 3) * 1024 +
+                                  (r & 7) * 128;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float* f = pv + 16 * h2;
+              st_shared_v4(prow + (((2 * q + h2) ^ (r & 7)) << 4),
+                           pack_e4m3x4(f[0], f[1], f[2], f[3]), pack_e4m3x4(f[4], f[5], f[6], f[7]),
+                           pack_e4m3x4(f[8], f[9], f[10], f[11]),
+                           pack_e4m3x4(f[12], f[13], f[14], f[15]));
+            }
+          } else {
+            tmem_st16(tS + q * 16, pk);
+          }
         }
+        if constexpr (FP8) fence_proxy_async_smem();  // P tile -> tensor-core operand
         {
           const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
           const float2 t = fadd2(a, b2);
@@ -571,7 +652,8 @@ __global__ void __launch_bounds__(384, 1)
       // O_i is in registers: the next item's first P V may overwrite it.
       tc_fence_before();
       mbar_arrive(&o_empty[i]);
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if constexpr (FP8) inv_l *= pow2i(-p.v_exp[static_cast<size_t>(it.b) * p.Hkv + it.hk]);
       if (row < it.n) {
         const size_t orow = (static_cast<size_t>(it.base) + row) * p.Hq + it.h;
 #pragma unroll

@@ -102,6 +102,73 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int o_dtype);
 
 /*
+ * FP8 (e4m3) prefill.  FlashAttention-3 computes attention in low-precision
+ * FP8 ("FlashAttention" learn page, aiunderstanding.org, section on the
+ * future of FlashAttention; FlashAttention-3 article, ybx.com,
+ * "FlashAttention-3 innovations" item 3).  The pages fix no format or scaling;
+ * this library uses:
+ *   - e4m3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *     infinities, largest finite value 448), conversion rounding to nearest
+ *     even and saturating at +-448;
+ *   - one int32 exponent e per tile: the largest e with amax * 2^e <= 448
+ *     (amax = max |x| over the tile; 0 for an all-zero tile; clamped to
+ *     [-126, 126]); a code c stands for c * 2^-e;
+ *   - tiles: Q and K per 128 rows (tokens) of one (batch, head); V per
+ *     (batch, head) over the whole sequence.  V is stored transposed,
+ *     [B, Hkv, d, Np] with Np = attn_fp8_padded_len(N) (N rounded up to 16),
+ *     keys N..Np-1 zero.
+ * d = 128 only; dense [B, N, H, d] layout only.
+ */
+
+/* attn_fp8_padded_len -- key-axis length Np of the transposed FP8 V (0 for N <= 0). */
+int attn_fp8_padded_len(int N);
+
+/*
+ * attn_fp8_workspace_size -- bytes of workspace attn_fp8_quantize needs (the
+ * f32 maximum of every 128-key tile of V, [B, Hkv, ceil(N/128)]), a multiple
+ * of 256; 256 on empty or invalid sizes.
+ */
+size_t attn_fp8_workspace_size(int B, int Hkv, int N);
+
+/*
+ * attn_fp8_quantize -- bf16 Q, K, V to e4m3 codes with per-tile exponents.
+ *
+ *   q          bf16 [B, N, Hq, d]      k, v  bf16 [B, N, Hkv, d]
+ *   q8         e4m3 [B, N, Hq, d]      k8    e4m3 [B, N, Hkv, d]
+ *   v8t        e4m3 [B, Hkv, d, Np]    (V transposed; Np as above)
+ *   q_exp      int32 [B, Hq, ceil(N/128)]   k_exp  int32 [B, Hkv, ceil(N/128)]
+ *   v_exp      int32 [B, Hkv]
+ *   workspace  >= attn_fp8_workspace_size(B, Hkv, N) bytes, 256-byte aligned
+ *   d == 128; Hq % Hkv == 0; q, k, v, q8, k8, v8t 16-byte aligned.
+ * Two kernel launches.  The outputs are a function of the inputs alone (no
+ * state, bit-identical on every call).
+ * Errors: INVALID, UNSUPPORTED (d), WORKSPACE, CUDA.
+ */
+int attn_fp8_quantize(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8t,
+                      int* q_exp, int* k_exp, int* v_exp, int B, int Hq, int Hkv, int N, int d,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_fwd_fp8 -- prefill attention on e4m3 operands from attn_fp8_quantize.
+ *
+ * The same tiled online-softmax computation as attn_fwd, with both tensor-core
+ * products in e4m3 and f32 accumulation: S = Q8 K8^T is scaled by
+ * scale * 2^-(e_Q + e_K) of its tile pair; the softmax numerators P (at most
+ * 2^8) are rounded to e4m3 before O += P V8; O is divided by the row sum and
+ * by 2^e_V.  LSE uses the unrounded numerators.
+ *
+ *   q8, k8, v8t, q_exp, k_exp, v_exp   as written by attn_fp8_quantize
+ *   o    [B, N, Hq, d], bf16 or f32 as o_dtype says
+ *   lse  f32 [B, Hq, N], natural logarithm
+ *   causal, window, scale as for attn_fwd; d == 128; one kernel launch.
+ * Errors: INVALID, UNSUPPORTED (d), CUDA.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const int* q_exp,
+                 const int* k_exp, const int* v_exp, void* o, float* lse, int B, int Hq, int Hkv,
+                 int N, int d, int causal, int window, float scale, cudaStream_t stream,
+                 int o_dtype);
+
+/*
  * attn_bwd_workspace_size -- bytes of workspace attn_bwd needs: the f32 row
  * terms D = rowsum(dO * O) [B, Hq, N], 256-byte aligned.  0 on invalid input.
  */

@@ -192,3 +192,37 @@ def test_paged_decode_validation(binding):
     assert call(ws=0) == WORKSPACE
     assert call(d=96) == UNSUPPORTED
     assert call(B=0, ptr=0, table=0, ws=0) == 0
+
+
+def test_fp8_validation(binding):
+    lib = binding.lib()
+    assert lib.attn_fp8_padded_len(1000) == 1008 and lib.attn_fp8_padded_len(4096) == 4096
+    assert lib.attn_fp8_padded_len(0) == 0
+    assert lib.attn_fp8_workspace_size(2, 4, 300) == 256  # 2*4*3 floats, rounded up to 256
+    assert lib.attn_fp8_workspace_size(4, 16, 4096) == 4 * 16 * 32 * 4
+
+    def quant(B=1, Hq=2, Hkv=2, N=16, d=128, ptr=FAKE, ws=FAKE, ws_bytes=1 << 20):
+        return lib.attn_fp8_quantize(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, B, Hq, Hkv, N,
+                                     d, ws, ws_bytes, None)
+    assert quant(B=-1) == INVALID
+    assert quant(Hq=3) == INVALID
+    assert quant(d=64) == UNSUPPORTED
+    assert quant(ptr=0) == INVALID
+    assert quant(ptr=FAKE + 8) == INVALID
+    assert quant(ws=0) == WORKSPACE
+    assert quant(ws_bytes=16) == WORKSPACE
+    assert quant(ws=FAKE + 16) == INVALID
+    assert quant(N=0, ptr=0, ws=0) == 0
+
+    def fwd(B=1, Hq=2, Hkv=2, N=16, d=128, ptr=FAKE, causal=0, scale=0.1, o_dtype=0):
+        return lib.attn_fwd_fp8(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, B, Hq, Hkv, N, d, causal,
+                                -1, scale, None, o_dtype)
+    assert fwd(B=-1) == INVALID
+    assert fwd(Hq=3) == INVALID
+    assert fwd(d=64) == UNSUPPORTED
+    assert fwd(ptr=0) == INVALID
+    assert fwd(ptr=FAKE + 4) == INVALID
+    assert fwd(causal=2) == INVALID
+    assert fwd(scale=float("nan")) == INVALID
+    assert fwd(o_dtype=7) == INVALID
+    assert fwd(B=0, ptr=0) == 0
