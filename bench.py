@@ -443,6 +443,9 @@ def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
     peak = peaks["bf16_tflops"]
     rf = roofline(tflops, peak, "TFLOP/s", "tensor", None, flops, "FLOP")
     rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
+    # traffic of the three launches is not one kernel's; the dK/dV kernel's own
+    # DRAM bytes (ncu) are reported beside the roofline
+    rf["traffic_bwd_dkdv_kernel"] = stored_traffic("bwd_dkdv_kernel", w.name + "_backward")
     return {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
             "launches_per_call": 3, "timing": timing,
             "config": dict(workload_config(w), workload=w.name + "_backward")}
