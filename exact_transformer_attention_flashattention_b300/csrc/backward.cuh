@@ -20,9 +20,12 @@
 // Splitting dQ from dK/dV recomputes S and dP once more but needs no atomics and
 // gives a deterministic result.
 //
-// CTA layout of the two tile kernels (256 threads): warp 0 TMA producer, warp 1
+// CTA layout of the two tile kernels (384 threads): warp 0 TMA producer, warp 1
 // MMA issuer (whole warp, one elected lane), warp 2 tensor-memory allocator,
-// warp 3 idle, warps 4-7 element-wise work (one tensor-memory lane = one row).
+// warp 3 idle, warps 4-11 element-wise work in two warpgroups: one
+// tensor-memory lane = one row, warpgroup 1 (warps 4-7) takes columns 0-63 of
+// the tile and warpgroup 2 (warps 8-11) columns 64-127, on packed f32x2
+// arithmetic.
 #pragma once
 
 #include "ptx.cuh"
@@ -85,13 +88,20 @@ __device__ __forceinline__ bool bwd_visible(int q, int k, int N, bool causal, in
   return true;
 }
 
+// Tensor-memory column of the bf16 pairs for 16-column group g (0..7) of a
+// 128-column f32 tile rewritten in place.  Each element-wise warpgroup packs
+// into the columns it reads (groups 0-3 into [0,32), groups 4-7 into
+// [64,96)), so neither overwrites f32 values the other has yet to read.
+__device__ __forceinline__ uint32_t packed_col(int g) { return g * 8 + (g >= 4 ? 32 : 0); }
+
 template <int D>
 struct BwdCfg {
   static constexpr int TILE = 128;                  // rows of a Q, dO, K or V tile
   static constexpr int DCH = D / 64;                // 128-byte swizzle atoms across d
   static constexpr int TILE_BYTES = TILE * D * 2;
   static constexpr int STAGES = 2;
-  static constexpr int THREADS = 256;
+  static constexpr int THREADS = 384;
+  static constexpr int EW_THREADS = 256;  // element-wise threads (two warpgroups)
 };
 
 // ---------------------------------------------------------------- dK, dV
@@ -108,7 +118,7 @@ struct DkdvSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
@@ -159,10 +169,10 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&ring_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, C::EW_THREADS);
     mbar_init(acc_done, 1);
-    mbar_init(&vec_full[0], 128);
-    mbar_init(&vec_full[1], 128);
+    mbar_init(&vec_full[0], C::EW_THREADS);
+    mbar_init(&vec_full[1], C::EW_THREADS);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -245,11 +255,11 @@ __global__ void __launch_bounds__(256, 1)
       const uint64_t doMN = qMN + static_cast<uint64_t>(C::TILE_BYTES >> 4);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tV, tS + kk * 8, doMN + ((kk * 16 * 128) >> 4), idO,
+        umma_ts_warp(tV, tS + packed_col(kk), doMN + ((kk * 16 * 128) >> 4), idO,
                      (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tK, tP + kk * 8, qMN + ((kk * 16 * 128) >> 4), idO,
+        umma_ts_warp(tK, tP + packed_col(kk), qMN + ((kk * 16 * 128) >> 4), idO,
                      (t > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&ring_empty[s]);
     }
@@ -258,25 +268,30 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp >= 4) {
     // ================================================================ element-wise
     const int quarter = warp & 3;
+    const int wg = (warp - 4) >> 2;     // 0: query columns 0-63, 1: columns 64-127
     const int r = quarter * 32 + lane;  // key row of this thread within the tile
     const int key = c0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     const bool causal = p.causal != 0;
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
       const int h = hk * G + t / nq;
       const int r0 = (ilo + t % nq) * 128;
-      // this step's per-query vectors: LSE (base 2) and D, staged in shared
-      // memory by the 128 threads (two slots; a slot is rewritten only after
-      // every thread has arrived for the step in between, i.e. read it)
-      float* lse2 = vec + (t & 1) * 256;
-      float* dvq = lse2 + 128;
+      // this step's per-query vectors, negated: -LSE (base 2) and -D, staged in
+      // shared memory (warpgroup 1 writes the first, warpgroup 2 the second;
+      // two slots; a slot is rewritten only after every element-wise thread
+      // has arrived for the step in between, i.e. finished reading it)
+      float* nlse = vec + (t & 1) * 256;
+      float* ndv = nlse + 128;
       {
         const int q = r0 + r;
         const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * N + q;
-        lse2[r] = (q < N) ? p.lse[vi] * kLog2e : 0.f;
-        dvq[r] = (q < N) ? p.dvec[vi] : 0.f;
+        if (wg == 0)
+          nlse[r] = (q < N) ? -p.lse[vi] * kLog2e : 0.f;
+        else
+          ndv[r] = (q < N) ? -p.dvec[vi] : 0.f;
       }
       mbar_arrive(&vec_full[t & 1]);
       ok = __all_sync(0xffffffffu, mbar_wait(&vec_full[t & 1], (t >> 1) & 1, &g_bwd_status,
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(256, 1)
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * wg; ch < 2 * wg + 2; ++ch) {
         uint32_t us[32], ud[32];
         tmem_ld32(tS + lane_off + ch * 32, us);
         tmem_ld32(tP + lane_off + ch * 32, ud);
@@ -299,23 +314,35 @@ __global__ void __launch_bounds__(256, 1)
         reg_fence(ud);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int col = ch * 32 + 2 * e + h2;
+        for (int e = 0; e < 16; e += 2) {  // four query columns per iteration
+          const int col = ch * 32 + 2 * e;
+          const float4 nl = *reinterpret_cast<const float4*>(nlse + col);
+          const float4 nd = *reinterpret_cast<const float4*>(ndv + col);
+          const float2 x0 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
+                                  sl2x2, make_float2(nl.x, nl.y));
+          const float2 x1 = ffma2(make_float2(__uint_as_float(us[2 * e + 2]), __uint_as_float(us[2 * e + 3])),
+                                  sl2x2, make_float2(nl.z, nl.w));
+          float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+          float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+          if (!full_tile) {
             const int q = r0 + col;
-            const bool vis = full_tile || bwd_visible(q, key, N, causal, p.window);
-            const float x = fmaf(__uint_as_float(us[2 * e + h2]), sl2, -lse2[col]);
-            const float pe = vis ? ex2_approx(x) : 0.f;
-            pv[h2] = pe;
-            dsv[h2] = pe * (__uint_as_float(ud[2 * e + h2]) - dvq[col]);
+            p0.x = bwd_visible(q, key, N, causal, p.window) ? p0.x : 0.f;
+            p0.y = bwd_visible(q + 1, key, N, causal, p.window) ? p0.y : 0.f;
+            p1.x = bwd_visible(q + 2, key, N, causal, p.window) ? p1.x : 0.f;
+            p1.y = bwd_visible(q + 3, key, N, causal, p.window) ? p1.y : 0.f;
           }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+          const float2 d0 = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
+                                  make_float2(nd.x, nd.y));
+          const float2 d1 = fadd2(make_float2(__uint_as_float(ud[2 * e + 2]), __uint_as_float(ud[2 * e + 3])),
+                                  make_float2(nd.z, nd.w));
+          const float2 ds0 = fmul2(p0, d0), ds1 = fmul2(p1, d1);
+          pk[e] = pack_bf16x2(p0.x, p0.y);
+          pk[e + 1] = pack_bf16x2(p1.x, p1.y);
+          dk[e] = pack_bf16x2(ds0.x, ds0.y);
+          dk[e + 1] = pack_bf16x2(ds1.x, ds1.y);
         }
-        tmem_st16(tS + lane_off + ch * 16, pk);
-        tmem_st16(tP + lane_off + ch * 16, dk);
+        tmem_st16(tS + lane_off + packed_col(2 * ch), pk);
+        tmem_st16(tP + lane_off + packed_col(2 * ch), dk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -328,8 +355,8 @@ __global__ void __launch_bounds__(256, 1)
       // every lane takes part in the (warp-collective) tensor-memory loads;
       // only rows inside the sequence are stored
       const size_t orow = (static_cast<size_t>(b) * N + min(key, N - 1)) * p.Hkv + hk;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = wg;  // warpgroup 1 stores dV, warpgroup 2 dK
         const uint32_t tA = (which ? tK : tV) + lane_off;
         const float mul = which ? p.scale : 1.f;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + orow * D;
@@ -374,7 +401,7 @@ struct DqSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -418,7 +445,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&ring_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, C::EW_THREADS);
     mbar_init(acc_done, 1);
     fence_mbar_init();
   }
@@ -498,7 +525,7 @@ __global__ void __launch_bounds__(256, 1)
       const uint64_t kMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tQ, tP + kk * 8, kMN + ((kk * 16 * 128) >> 4), idO,
+        umma_ts_warp(tQ, tP + packed_col(kk), kMN + ((kk * 16 * 128) >> 4), idO,
                      (t > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&ring_empty[s]);
     }
@@ -507,14 +534,17 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp >= 4) {
     // ================================================================ element-wise
     const int quarter = warp & 3;
+    const int wg = (warp - 4) >> 2;     // 0: key columns 0-63, 1: columns 64-127
     const int r = quarter * 32 + lane;  // query row of this thread within the tile
     const int row = r0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * N + row;
-    const float lse2 = (row < N) ? p.lse[vi] * kLog2e : 0.f;
-    const float drow = (row < N) ? p.dvec[vi] : 0.f;
+    const float nlse = (row < N) ? -p.lse[vi] * kLog2e : 0.f;
+    const float ndrow = (row < N) ? -p.dvec[vi] : 0.f;
+    const float2 sl2x2 = make_float2(sl2, sl2), nlse2 = make_float2(nlse, nlse);
+    const float2 ndrow2 = make_float2(ndrow, ndrow);
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
       const int c0 = (jlo + t) * 128;
@@ -526,7 +556,7 @@ __global__ void __launch_bounds__(256, 1)
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * wg; ch < 2 * wg + 2; ++ch) {
         uint32_t us[32], ud[32];
         tmem_ld32(tS + lane_off + ch * 32, us);
         tmem_ld32(tP + lane_off + ch * 32, ud);
@@ -536,18 +566,20 @@ __global__ void __launch_bounds__(256, 1)
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float dsv[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int key = c0 + ch * 32 + 2 * e + h2;
-            const bool vis = full_tile || bwd_visible(row, key, N, causal, p.window);
-            const float x = fmaf(__uint_as_float(us[2 * e + h2]), sl2, -lse2);
-            const float pe = vis ? ex2_approx(x) : 0.f;
-            dsv[h2] = pe * (__uint_as_float(ud[2 * e + h2]) - drow);
+          const float2 x = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
+                                 sl2x2, nlse2);
+          float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (!full_tile) {
+            const int key = c0 + ch * 32 + 2 * e;
+            pe.x = bwd_visible(row, key, N, causal, p.window) ? pe.x : 0.f;
+            pe.y = bwd_visible(row, key + 1, N, causal, p.window) ? pe.y : 0.f;
           }
-          dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+          const float2 dd = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
+                                  ndrow2);
+          const float2 ds = fmul2(pe, dd);
+          dk[e] = pack_bf16x2(ds.x, ds.y);
         }
-        tmem_st16(tP + lane_off + ch * 16, dk);
+        tmem_st16(tP + lane_off + packed_col(2 * ch), dk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -562,7 +594,7 @@ __global__ void __launch_bounds__(256, 1)
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dq) +
                            ((static_cast<size_t>(b) * N + min(row, N - 1)) * p.Hq + h) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = wg * (D / 64); cc < (wg + 1) * (D / 64); ++cc) {  // half of d per warpgroup
         uint32_t u[32];
         tmem_ld32_wait(tQ + lane_off + cc * 32, u);
         if (row >= N) continue;
