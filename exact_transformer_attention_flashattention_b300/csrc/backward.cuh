@@ -275,24 +275,25 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     const bool causal = p.causal != 0;
+    // this thread's entry of step t's per-query vector, negated: -LSE (base 2)
+    // from warpgroup 1, -D from warpgroup 2; loaded one step ahead
+    auto vec_entry = [&](int t) -> float {
+      const int q = (ilo + t % nq) * 128 + r;
+      const size_t vi = (static_cast<size_t>(b) * p.Hq + hk * G + t / nq) * N + q;
+      if (q >= N) return 0.f;
+      return wg == 0 ? -p.lse[vi] * kLog2e : -p.dvec[vi];
+    };
+    float v_next = nsteps > 0 ? vec_entry(0) : 0.f;
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
-      const int h = hk * G + t / nq;
       const int r0 = (ilo + t % nq) * 128;
-      // this step's per-query vectors, negated: -LSE (base 2) and -D, staged in
-      // shared memory (warpgroup 1 writes the first, warpgroup 2 the second;
-      // two slots; a slot is rewritten only after every element-wise thread
-      // has arrived for the step in between, i.e. finished reading it)
+      // the step's vectors are staged in shared memory (two slots; a slot is
+      // rewritten only after every element-wise thread has arrived for the
+      // step in between, i.e. finished reading it)
       float* nlse = vec + (t & 1) * 256;
       float* ndv = nlse + 128;
-      {
-        const int q = r0 + r;
-        const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * N + q;
-        if (wg == 0)
-          nlse[r] = (q < N) ? -p.lse[vi] * kLog2e : 0.f;
-        else
-          ndv[r] = (q < N) ? -p.dvec[vi] : 0.f;
-      }
+      (wg == 0 ? nlse : ndv)[r] = v_next;
+      if (t + 1 < nsteps) v_next = vec_entry(t + 1);
       mbar_arrive(&vec_full[t & 1]);
       ok = __all_sync(0xffffffffu, mbar_wait(&vec_full[t & 1], (t >> 1) & 1, &g_bwd_status,
                                              kStatusBwdVec));

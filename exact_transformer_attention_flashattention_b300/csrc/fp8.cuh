@@ -150,26 +150,31 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   const int hk = static_cast<int>((job / p.nt) % p.Hkv);
   const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * p.Hkv));
   const size_t bh = static_cast<size_t>(b) * p.Hkv + hk;
+  // Transposing mapping: lane = group of 4 consecutive keys (4*lane .. 4*lane+3),
+  // warp w covers 8 elements of d at w*8 and w*8 + 64.  Each thread packs the
+  // 4 keys of one d into a 32-bit word of the transposed tile.  The tile's
+  // loads are issued before the head's maximum is reduced, so both are in
+  // flight together.
+  const int rg = tid & 31, cg = tid >> 5;
+  uint4 wt[2][4];
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = t * 128 + 4 * rg + i;
+      wt[pass][i] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < p.N) wt[pass][i] = tile_row_ptr<D>(p.v, b, hk, p.Hkv, p.N, row)[cg + 8 * pass];
+    }
   float m = 0.f;
   for (int u = tid; u < p.nt; u += kFp8QuantThreads) m = fmaxf(m, p.v_tile_amax[bh * p.nt + u]);
   m = block_max256(m, red);
   const int e = fp8_scale_exponent(m);
   const float s = pow2i(e);
   if (tid == 0 && t == 0) p.v_exp[bh] = e;
-  // Transposing mapping: lane = group of 4 consecutive keys (4*lane .. 4*lane+3),
-  // warp w covers 8 elements of d at w*8 and w*8 + 64.  Each thread packs the
-  // 4 keys of one d into a 32-bit word of the transposed tile.
-  const int rg = tid & 31, cg = tid >> 5;
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     const int c8 = cg + 8 * pass;  // 16-byte column of d
-    uint4 w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = t * 128 + 4 * rg + i;
-      w[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (row < p.N) w[i] = tile_row_ptr<D>(p.v, b, hk, p.Hkv, p.N, row)[c8];
-    }
+    const uint4* w = wt[pass];
     float f[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
