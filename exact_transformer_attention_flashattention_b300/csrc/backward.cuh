@@ -22,10 +22,16 @@
 //
 // CTA layout of the two tile kernels (384 threads): warp 0 TMA producer, warp 1
 // MMA issuer (whole warp, one elected lane), warp 2 tensor-memory allocator,
-// warp 3 idle, warps 4-11 element-wise work in two warpgroups: one
-// tensor-memory lane = one row, warpgroup 1 (warps 4-7) takes columns 0-63 of
-// the tile and warpgroup 2 (warps 8-11) columns 64-127, on packed f32x2
-// arithmetic.
+// warp 3 idle, warps 4-11 element-wise work in two warpgroups (one
+// tensor-memory lane = one row, packed f32x2 arithmetic).
+//
+// Each streamed 128-row tile is handled as two halves of 64 columns, each with
+// its own S and dP in tensor memory and its own element-wise warpgroup.  The
+// MMA order per tile t
+//   [S, dP of both halves of t issued earlier]  grad(half 0, t)  S, dP(half 0, t+1)
+//   grad(half 1, t)  S, dP(half 1, t+1)
+// lets one half's element-wise pass run while the tensor core works on the
+// other half, as the forward does with its two query tiles.
 #pragma once
 
 #include "ptx.cuh"
@@ -88,12 +94,6 @@ __device__ __forceinline__ bool bwd_visible(int q, int k, int N, bool causal, in
   return true;
 }
 
-// Tensor-memory column of the bf16 pairs for 16-column group g (0..7) of a
-// 128-column f32 tile rewritten in place.  Each element-wise warpgroup packs
-// into the columns it reads (groups 0-3 into [0,32), groups 4-7 into
-// [64,96)), so neither overwrites f32 values the other has yet to read.
-__device__ __forceinline__ uint32_t packed_col(int g) { return g * 8 + (g >= 4 ? 32 : 0); }
-
 template <int D>
 struct BwdCfg {
   static constexpr int TILE = 128;                  // rows of a Q, dO, K or V tile
@@ -133,10 +133,10 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* kv_full = bars;                // K_j, V_j landed
   uint64_t* ring_full = bars + 1;          // [STAGES]
   uint64_t* ring_empty = ring_full + STAGES;
-  uint64_t* s_full = ring_empty + STAGES;  // S^T and dP^T in tensor memory
-  uint64_t* p_ready = s_full + 1;          // P^T, dS^T written by the 128 compute threads
-  uint64_t* acc_done = p_ready + 1;        // every MMA done
-  uint64_t* vec_full = acc_done + 1;       // [2] per-query vectors staged (128 threads)
+  uint64_t* s_full = ring_empty + STAGES;  // [2] S^T and dP^T of query half w in tensor memory
+  uint64_t* p_ready = s_full + 2;          // [2] P^T, dS^T of half w written (128 threads)
+  uint64_t* acc_done = p_ready + 2;        // every MMA done
+  uint64_t* vec_full = acc_done + 1;       // [2] per-query vectors staged (256 threads)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,8 +168,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&ring_full[s], 1);
       mbar_init(&ring_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, C::EW_THREADS);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&s_full[w], 1);
+      mbar_init(&p_ready[w], C::EW_THREADS / 2);
+    }
     mbar_init(acc_done, 1);
     mbar_init(&vec_full[0], C::EW_THREADS);
     mbar_init(&vec_full[1], C::EW_THREADS);
@@ -183,8 +185,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // tensor memory: S^T [0,128)  dP^T [128,256)  dV [256,256+D)  dK [256+D,256+2D)
-  const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 256 + D;
+  // tensor memory: query half w (64 queries) has S^T at [128w, 128w+64) and dP^T
+  // at [128w+64, 128w+128); dV [256,256+D)  dK [256+D,256+2D)
+  const uint32_t tV = tmem + 256, tK = tmem + 256 + D;
 
   if (warp == 0) {
     // ================================================================ producer
@@ -218,59 +221,80 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    const uint32_t idS = idesc_bf16_f32(128, 128, false);
+    const uint32_t idS = idesc_bf16_f32(128, 64, false);  // 128 keys x 64 queries
     const uint32_t idO = idesc_bf16_f32(128, D, true);
     const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
     const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + L::V_OFF), 16, 1024);
     const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 16, 1024);
     const uint64_t dRmn = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 128 * 128, 1024);
-    auto wait = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, kStatusBwdMma));
+    auto wait = [&](uint64_t* bar, uint32_t parity, unsigned site) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, site));
     };
-    bool ok = wait(kv_full, 0);
-    for (int t = 0; t < nsteps && ok; ++t) {
-      const int s = t % STAGES;
-      if (!(ok = wait(&ring_full[s], (t / STAGES) & 1))) break;
-      tc_fence_after();
-      const uint64_t qK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+    // S^T_w = K Q_w^T and dP^T_w = V dO_w^T for query half w: rows 64w.. of the
+    // stage's Q / dO tiles, 8 KB into each 128-byte-wide block (a whole number
+    // of 1 KB swizzle atoms)
+    auto issue_sdp = [&](int w, int s) {
+      const uint64_t qK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES + w * 64 * 128) >> 4);
       const uint64_t doK = qK + static_cast<uint64_t>(C::TILE_BYTES >> 4);
-      // S^T = K Q^T and dP^T = V dO^T (keys on the lanes, queries on the columns)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tS, dK0 + off, qK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ss_warp(tmem + 128 * w, dK0 + off, qK + off, idS, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tP, dV0 + off, doK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ss_warp(tmem + 128 * w + 64, dV0 + off, doK + off, idS, kk > 0 ? 1u : 0u);
       }
-      umma_commit_warp(s_full);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, &g_bwd_status,
-                                                   kStatusBwdMmaP)))) break;
-      tc_fence_after();
-      // dV += P^T dO and dK += dS^T Q: A from tensor memory (bf16 pairs), B the
-      // stage's dO / Q tile read MN-major, 16 queries per instruction
+      umma_commit_warp(&s_full[w]);
+    };
+    // dV += P^T_w dO_w and dK += dS^T_w Q_w: A from tensor memory (the half's
+    // bf16 pairs, in the first 32 columns of its S^T / dP^T), B the stage's
+    // dO / Q rows of the half read MN-major, 16 queries per instruction
+    auto issue_grad = [&](int w, int s, bool first) {
       const uint64_t qMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
       const uint64_t doMN = qMN + static_cast<uint64_t>(C::TILE_BYTES >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tV, tS + packed_col(kk), doMN + ((kk * 16 * 128) >> 4), idO,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+      for (int k4 = 0; k4 < 4; ++k4)
+        umma_ts_warp(tV, tmem + 128 * w + k4 * 8, doMN + (((4 * w + k4) * 16 * 128) >> 4), idO,
+                     (!first || k4 > 0) ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tK, tP + packed_col(kk), qMN + ((kk * 16 * 128) >> 4), idO,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+      for (int k4 = 0; k4 < 4; ++k4)
+        umma_ts_warp(tK, tmem + 128 * w + 64 + k4 * 8, qMN + (((4 * w + k4) * 16 * 128) >> 4),
+                     idO, (!first || k4 > 0) ? 1u : 0u);
+    };
+    bool ok = wait(kv_full, 0, kStatusBwdMma);
+    if (ok && nsteps > 0 && (ok = wait(&ring_full[0], 0, kStatusBwdMma))) {
+      tc_fence_after();
+      issue_sdp(0, 0);
+      issue_sdp(1, 0);
+    }
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int s = t % STAGES, s1 = (t + 1) % STAGES;
+      const bool has_next = t + 1 < nsteps;
+      if (!(ok = wait(&p_ready[0], t & 1, kStatusBwdMmaP))) break;
+      tc_fence_after();
+      issue_grad(0, s, t == 0);
+      if (has_next) {
+        if (!(ok = wait(&ring_full[s1], ((t + 1) / STAGES) & 1, kStatusBwdMma))) break;
+        tc_fence_after();
+        issue_sdp(0, s1);
+      }
+      if (!(ok = wait(&p_ready[1], t & 1, kStatusBwdMmaP))) break;
+      tc_fence_after();
+      issue_grad(1, s, false);
       umma_commit_warp(&ring_empty[s]);
+      if (has_next) issue_sdp(1, s1);
     }
     umma_commit_warp(acc_done);
-    wait(acc_done, 0);
+    wait(acc_done, 0, kStatusBwdMma);
   } else if (warp >= 4) {
     // ================================================================ element-wise
     const int quarter = warp & 3;
-    const int wg = (warp - 4) >> 2;     // 0: query columns 0-63, 1: columns 64-127
+    const int wg = (warp - 4) >> 2;     // query half: columns 64*wg .. 64*wg+63 of the tile
     const int r = quarter * 32 + lane;  // key row of this thread within the tile
     const int key = c0 + r;
+    const uint32_t tS = tmem + 128 * wg, tP = tS + 64;  // this half's S^T and dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
@@ -298,15 +322,18 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&vec_full[t & 1], (t >> 1) & 1, &g_bwd_status,
                                              kStatusBwdVec));
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, &g_bwd_status, kStatusBwdCompute));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], t & 1, &g_bwd_status,
+                                             kStatusBwdCompute));
       if (!ok) break;
       tc_fence_after();
       const bool full_tile = (r0 + 127 < N) && (c0 + 127 < N) &&
                              (!causal || r0 >= c0 + 127) &&
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
+      // two chunks of 32 columns; chunk ch's bf16 pairs go to columns
+      // [16ch, 16ch+16) of the same array, already read by then
 #pragma unroll 1
-      for (int ch = 2 * wg; ch < 2 * wg + 2; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t us[32], ud[32];
         tmem_ld32(tS + lane_off + ch * 32, us);
         tmem_ld32(tP + lane_off + ch * 32, ud);
@@ -316,7 +343,7 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {  // four query columns per iteration
-          const int col = ch * 32 + 2 * e;
+          const int col = 64 * wg + ch * 32 + 2 * e;
           const float4 nl = *reinterpret_cast<const float4*>(nlse + col);
           const float4 nd = *reinterpret_cast<const float4*>(ndv + col);
           const float2 x0 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
@@ -342,12 +369,12 @@ __global__ void __launch_bounds__(384, 1)
           dk[e] = pack_bf16x2(ds0.x, ds0.y);
           dk[e + 1] = pack_bf16x2(ds1.x, ds1.y);
         }
-        tmem_st16(tS + lane_off + packed_col(2 * ch), pk);
-        tmem_st16(tP + lane_off + packed_col(2 * ch), dk);
+        tmem_st16(tS + lane_off + ch * 16, pk);
+        tmem_st16(tP + lane_off + ch * 16, dk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[wg]);
     }
     // ---------------------------------------------------------- epilogue
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, &g_bwd_status, kStatusBwdEpilogue));
@@ -416,9 +443,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars;                 // Q_i, dO_i landed
   uint64_t* ring_full = bars + 1;          // [STAGES]
   uint64_t* ring_empty = ring_full + STAGES;
-  uint64_t* s_full = ring_empty + STAGES;
-  uint64_t* p_ready = s_full + 1;
-  uint64_t* acc_done = p_ready + 1;
+  uint64_t* s_full = ring_empty + STAGES;  // [2] S and dP of key half w in tensor memory
+  uint64_t* p_ready = s_full + 2;          // [2] dS of half w written (128 threads)
+  uint64_t* acc_done = p_ready + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -445,8 +472,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&ring_full[s], 1);
       mbar_init(&ring_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, C::EW_THREADS);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&s_full[w], 1);
+      mbar_init(&p_ready[w], C::EW_THREADS / 2);
+    }
     mbar_init(acc_done, 1);
     fence_mbar_init();
   }
@@ -458,8 +487,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // tensor memory: S [0,128)  dP [128,256)  dQ [256,256+D)
-  const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+  // tensor memory: key half w (64 keys) has S at [128w, 128w+64) and dP at
+  // [128w+64, 128w+128); dQ [256,256+D)
+  const uint32_t tQ = tmem + 256;
 
   if (warp == 0) {
     // ================================================================ producer
@@ -492,52 +522,73 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    const uint32_t idS = idesc_bf16_f32(128, 128, false);
+    const uint32_t idS = idesc_bf16_f32(128, 64, false);  // 128 queries x 64 keys
     const uint32_t idO = idesc_bf16_f32(128, D, true);
     const uint64_t dQ0 = smem_desc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
     const uint64_t dDO0 = smem_desc_sw128(smem_u32(smem + L::DO_OFF), 16, 1024);
     const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 16, 1024);
     const uint64_t dRmn = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 128 * 128, 1024);
-    auto wait = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, kStatusBwdMma));
+    auto wait = [&](uint64_t* bar, uint32_t parity, unsigned site) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &g_bwd_status, site));
     };
-    bool ok = wait(q_full, 0);
-    for (int t = 0; t < nsteps && ok; ++t) {
-      const int s = t % STAGES;
-      if (!(ok = wait(&ring_full[s], (t / STAGES) & 1))) break;
-      tc_fence_after();
-      const uint64_t kK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
+    // S_w = Q K_w^T and dP_w = dO V_w^T for key half w: rows 64w.. of the
+    // stage's K / V tiles (8 KB into each 128-byte-wide block)
+    auto issue_sdp = [&](int w, int s) {
+      const uint64_t kK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES + w * 64 * 128) >> 4);
       const uint64_t vK = kK + static_cast<uint64_t>(C::TILE_BYTES >> 4);
-      // S = Q K^T and dP = dO V^T (queries on the lanes, keys on the columns)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tS, dQ0 + off, kK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ss_warp(tmem + 128 * w, dQ0 + off, kK + off, idS, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tP, dDO0 + off, vK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ss_warp(tmem + 128 * w + 64, dDO0 + off, vK + off, idS, kk > 0 ? 1u : 0u);
       }
-      umma_commit_warp(s_full);
-      if (!(ok = wait(p_ready, t & 1))) break;
-      tc_fence_after();
-      // dQ += dS K: dS (bf16 pairs) from tensor memory, the stage's K tile read MN-major
+      umma_commit_warp(&s_full[w]);
+    };
+    // dQ += dS_w K_w: dS (bf16 pairs in the first 32 columns of the half's dP)
+    // from tensor memory, the stage's K rows of the half read MN-major
+    auto issue_grad = [&](int w, int s, bool first) {
       const uint64_t kMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ts_warp(tQ, tP + packed_col(kk), kMN + ((kk * 16 * 128) >> 4), idO,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+      for (int k4 = 0; k4 < 4; ++k4)
+        umma_ts_warp(tQ, tmem + 128 * w + 64 + k4 * 8, kMN + (((4 * w + k4) * 16 * 128) >> 4),
+                     idO, (!first || k4 > 0) ? 1u : 0u);
+    };
+    bool ok = wait(q_full, 0, kStatusBwdMma);
+    if (ok && nsteps > 0 && (ok = wait(&ring_full[0], 0, kStatusBwdMma))) {
+      tc_fence_after();
+      issue_sdp(0, 0);
+      issue_sdp(1, 0);
+    }
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int s = t % STAGES, s1 = (t + 1) % STAGES;
+      const bool has_next = t + 1 < nsteps;
+      if (!(ok = wait(&p_ready[0], t & 1, kStatusBwdMmaP))) break;
+      tc_fence_after();
+      issue_grad(0, s, t == 0);
+      if (has_next) {
+        if (!(ok = wait(&ring_full[s1], ((t + 1) / STAGES) & 1, kStatusBwdMma))) break;
+        tc_fence_after();
+        issue_sdp(0, s1);
+      }
+      if (!(ok = wait(&p_ready[1], t & 1, kStatusBwdMmaP))) break;
+      tc_fence_after();
+      issue_grad(1, s, false);
       umma_commit_warp(&ring_empty[s]);
+      if (has_next) issue_sdp(1, s1);
     }
     umma_commit_warp(acc_done);
-    wait(acc_done, 0);
+    wait(acc_done, 0, kStatusBwdMma);
   } else if (warp >= 4) {
     // ================================================================ element-wise
     const int quarter = warp & 3;
-    const int wg = (warp - 4) >> 2;     // 0: key columns 0-63, 1: columns 64-127
+    const int wg = (warp - 4) >> 2;     // key half: columns 64*wg .. 64*wg+63 of the tile
     const int r = quarter * 32 + lane;  // query row of this thread within the tile
     const int row = r0 + r;
+    const uint32_t tS = tmem + 128 * wg, tP = tS + 64;  // this half's S and dP
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
@@ -549,15 +600,18 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
       const int c0 = (jlo + t) * 128;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, &g_bwd_status, kStatusBwdCompute));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], t & 1, &g_bwd_status,
+                                             kStatusBwdCompute));
       if (!ok) break;
       tc_fence_after();
       const bool full_tile = (r0 + 127 < N) && (c0 + 127 < N) &&
                              (!causal || r0 >= c0 + 127) &&
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
+      // two chunks of 32 columns; chunk ch's bf16 pairs go to columns
+      // [16ch, 16ch+16) of the half's dP, already read by then
 #pragma unroll 1
-      for (int ch = 2 * wg; ch < 2 * wg + 2; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t us[32], ud[32];
         tmem_ld32(tS + lane_off + ch * 32, us);
         tmem_ld32(tP + lane_off + ch * 32, ud);
@@ -571,7 +625,7 @@ __global__ void __launch_bounds__(384, 1)
                                  sl2x2, nlse2);
           float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (!full_tile) {
-            const int key = c0 + ch * 32 + 2 * e;
+            const int key = c0 + 64 * wg + ch * 32 + 2 * e;
             pe.x = bwd_visible(row, key, N, causal, p.window) ? pe.x : 0.f;
             pe.y = bwd_visible(row, key + 1, N, causal, p.window) ? pe.y : 0.f;
           }
@@ -580,11 +634,11 @@ __global__ void __launch_bounds__(384, 1)
           const float2 ds = fmul2(pe, dd);
           dk[e] = pack_bf16x2(ds.x, ds.y);
         }
-        tmem_st16(tP + lane_off + packed_col(2 * ch), dk);
+        tmem_st16(tP + lane_off + ch * 16, dk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[wg]);
     }
     // ---------------------------------------------------------- epilogue
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, &g_bwd_status, kStatusBwdEpilogue));
