@@ -226,3 +226,19 @@ def test_fp8_validation(binding):
     assert fwd(scale=float("nan")) == INVALID
     assert fwd(o_dtype=7) == INVALID
     assert fwd(B=0, ptr=0) == 0
+
+
+def test_binding_rejects_host_and_mistyped_tensors(binding):
+    """The Python wrappers refuse host tensors and wrong dtypes before any call."""
+    import torch
+    q = torch.zeros(1, 16, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.attn_fwd(q, q, q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.attn_fp8_quantize(q, q, q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.attn_fwd_fp8({"q8": q.to(torch.uint8), "k8": q.to(torch.uint8),
+                              "v8t": q.to(torch.uint8), "q_exp": None, "k_exp": None,
+                              "v_exp": None})
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.attn_bwd(q, q, q, q, torch.zeros(1, 2, 16), q)
