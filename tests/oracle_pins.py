@@ -407,10 +407,102 @@ def pin_backward_torch_autograd(orc, seed=15):
         _close(dV, tv.grad.numpy(), 1e-12, f"autograd dV {causal} {window}")
 
 
+def brute_decode(q, kc, vc, kv_len, scale):
+    """Scalar loops for single-query decode: query head h of sequence b scores
+    keys 0 .. kv_len[b]-1 of kv head h // (Hq / Hkv) with math.exp."""
+    B, Hq, d = q.shape
+    Hkv = kc.shape[2]
+    dv = vc.shape[3]
+    G = Hq // Hkv
+    O = np.zeros((B, Hq, dv))
+    LSE = np.full((B, Hq), -math.inf)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            scores = []
+            for j in range(int(kv_len[b])):
+                s = 0.0
+                for t in range(d):
+                    s += float(q[b, h, t]) * float(kc[b, j, hk, t])
+                scores.append(scale * s)
+            if not scores:
+                continue
+            top = max(scores)
+            ws = [math.exp(s - top) for s in scores]
+            Z = sum(ws)
+            for t in range(dv):
+                O[b, h, t] = sum(w * float(vc[b, j, hk, t]) for j, w in enumerate(ws)) / Z
+            LSE[b, h] = top + math.log(Z)
+    return O, LSE
+
+
+def pin_attention_rows_bruteforce(orc, seed=16):
+    """``attention_rows`` (the spot-check form used on full-size launches)
+    against the brute-force loop on the same rows: unsorted row lists that
+    include the first and the last row, every mask kind, grouped heads with
+    Hq / Hkv = 3, several batches, numpy and torch bf16 inputs."""
+    rng = np.random.default_rng(seed)
+    cases = [
+        (2, 11, 6, 2, 3, False, -1, 0.7),
+        (2, 12, 6, 2, 4, True, -1, 0.5),
+        (2, 10, 3, 1, 3, False, 2, 1.2),
+        (2, 13, 6, 2, 3, True, 3, 0.9),
+    ]
+    for B, N, Hq, Hkv, d, causal, window, scale in cases:
+        q = _rand((B, N, Hq, d), rng)
+        k = _rand((B, N, Hkv, d), rng)
+        v = _rand((B, N, Hkv, d + 2), rng)
+        Ob, Lb = brute_attention(q, k, v, causal, window, scale)
+        rows = [N - 1, 0, N // 2, 3, 1]
+        for b in range(B):
+            for h in range(Hq):
+                O, L = orc.attention_rows(q, k, v, b, h, rows, causal=causal, window=window,
+                                          scale=scale)
+                _close(O, Ob[b, rows, h], 1e-12, f"rows O b{b} h{h} {causal} {window}")
+                _close(L, Lb[b, h, rows], 1e-12, f"rows LSE b{b} h{h} {causal} {window}")
+    # torch bf16 inputs (what the GPU tests pass) go through the same path
+    qt = torch.randn(1, 9, 3, 4, generator=torch.Generator().manual_seed(seed)).bfloat16()
+    kt = torch.randn(1, 9, 1, 4, generator=torch.Generator().manual_seed(seed + 1)).bfloat16()
+    vt = torch.randn(1, 9, 1, 4, generator=torch.Generator().manual_seed(seed + 2)).bfloat16()
+    Ob, Lb = brute_attention(qt.double().numpy(), kt.double().numpy(), vt.double().numpy(),
+                             True, -1, 0.5)
+    O, L = orc.attention_rows(qt, kt, vt, 0, 2, [8, 0, 4], causal=True, scale=0.5)
+    _close(O, Ob[0, [8, 0, 4], 2], 1e-12, "rows bf16 O")
+    _close(L, Lb[0, 2, [8, 0, 4]], 1e-12, "rows bf16 LSE")
+
+
+def pin_decode_heads_subset(orc, seed=17):
+    """``decode`` against the brute-force decode loop, for all heads and for a
+    scrambled subset of (sequence, head) pairs that hops between sequences and
+    kv heads (so any cache of the per-(sequence, kv head) keys must be rebuilt
+    between them); pairs outside the subset stay zero.  Ragged lengths include
+    a one-key sequence."""
+    rng = np.random.default_rng(seed)
+    for B, Hq, Hkv, L, d, kv_len in [(3, 6, 2, 14, 3, [9, 1, 14]),
+                                     (2, 8, 2, 11, 4, [11, 6])]:
+        q = _rand((B, Hq, d), rng)
+        kc, vc = _rand((B, L, Hkv, d), rng), _rand((B, L, Hkv, d + 1), rng)
+        kv = np.array(kv_len)
+        Ob, Lb = brute_decode(q, kc, vc, kv, 0.8)
+        O, LSE = orc.decode(q, kc, vc, kv, scale=0.8)
+        _close(O, Ob, 1e-12, "decode O all heads")
+        _close(LSE, Lb, 1e-12, "decode LSE all heads")
+        pairs = [(B - 1, Hq - 1), (0, 0), (B - 1, 1), (1, Hq // 2), (0, Hq - 2), (B - 1, Hq // 2),
+                 (0, 1)]
+        O, LSE = orc.decode(q, kc, vc, kv, scale=0.8, heads=pairs)
+        for b in range(B):
+            for h in range(Hq):
+                if (b, h) in pairs:
+                    _close(O[b, h], Ob[b, h], 1e-12, f"decode subset O b{b} h{h}")
+                    _close(LSE[b, h], Lb[b, h], 1e-12, f"decode subset LSE b{b} h{h}")
+                else:
+                    assert np.all(O[b, h] == 0.0) and LSE[b, h] == 0.0, "untouched pair"
+
+
 ALL_PINS = [
     pin_bruteforce, pin_torch_sdpa, pin_rows_sum_to_one, pin_constant_v, pin_single_key,
     pin_causal_first_row, pin_window_limits, pin_scale_zero, pin_hardmax_limit,
     pin_key_permutation, pin_gqa_mapping, pin_band_equals_dense, pin_golden,
     pin_split_merge, pin_empty_rows, pin_varlen_bruteforce, pin_backward_finite_differences,
-    pin_backward_torch_autograd,
+    pin_backward_torch_autograd, pin_attention_rows_bruteforce, pin_decode_heads_subset,
 ]

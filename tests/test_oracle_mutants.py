@@ -38,6 +38,18 @@ MUTANTS = [
     ("bwd_gqa_overwrites", "dK[b, :, hk] += scale", "dK[b, :, hk] = scale"),
     ("empty_row_lse_zero", "lse = np.where(empty, NEG_INF, m_safe + np.log(l_safe))",
      "lse = np.where(empty, 0.0, m_safe + np.log(l_safe))"),
+    # the spot-check and head-subset forms used on full-size launches
+    ("rows_mask_shifted", "vis = visible(N, N, causal, window)[rows]",
+     "vis = visible(N, N, causal, window)[rows - 1]"),
+    ("rows_wrong_kv_head", "hk = h // (Hq // Hkv)", "hk = h % Hkv"),
+    ("rows_first_batch", "_f64(q[b, rows, h])", "_f64(q[0, rows, h])"),
+    ("decode_cache_reused", "if (b, hk) not in cached:", "if not cached:"),
+    ("decode_cache_kept_per_batch", "if (b, hk) not in cached:",
+     "if b not in [key[0] for key in cached]:"),
+    ("decode_first_length", "n = int(kv_len[b])\n        hk = h // G\n        if (b, hk)",
+     "n = int(kv_len[0])\n        hk = h // G\n        if (b, hk)"),
+    ("decode_gqa_modulo", "hk = h // G\n        if (b, hk) not in cached",
+     "hk = h % Hkv\n        if (b, hk) not in cached"),
 ]
 
 
