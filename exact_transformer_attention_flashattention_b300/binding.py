@@ -46,6 +46,7 @@ SIGNATURES = {
     "attn_decode_partials": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "lse_tree_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I]),
     "attn_device_status": (_I, [_P]),
+    "attn_selftest_bounded_wait": (_I, [ctypes.c_ulonglong, _P]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_version": (_I, []),
 }
@@ -410,6 +411,12 @@ def lse_tree_combine(part_m, part_l, part_o, out=None, lse=None, out_dtype=torch
 def device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the library's device status."""
     return int(_lib.attn_device_status(_stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch the library's failure-path self-test: a wait that nothing ends
+    gives up after ``limit_ns``; the next ``device_status`` reports it."""
+    _check(_lib.attn_selftest_bounded_wait(int(limit_ns), _stream(stream)))
 
 
 def last_error() -> str:

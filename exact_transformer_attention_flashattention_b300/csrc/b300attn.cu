@@ -388,6 +388,22 @@ int noalloc_scratch(void** out) {
   return B300ATTN_OK;
 }
 
+// Self-test of the failure path: one thread waits on an mbarrier that nothing
+// ever arrives on, with no copy or MMA in flight, so the bounded wait must run
+// out after `limit_ns` and record its bit; the CTA then returns normally.
+__device__ unsigned int g_selftest_status;
+constexpr unsigned kStatusSelftest = 1u;
+
+__global__ void __launch_bounds__(32) selftest_wait_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &g_selftest_status, kStatusSelftest, limit_ns);
+}
+
 }  // namespace
 
 extern "C" {
@@ -777,23 +793,39 @@ int lse_tree_combine(const float* part_m, const float* part_l, const float* part
                         o_dtype == B300ATTN_F32, stream);
 }
 
+int attn_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 100000000ull)
+    return fail(B300ATTN_ERR_INVALID, "limit_ns=%llu must lie in [1e3, 1e8] (1 us .. 100 ms)",
+                limit_ns);
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return B300ATTN_OK;
+}
+
 int attn_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int a = 0, b = 0, c = 0;
+  unsigned int a = 0, b = 0, c = 0, t = 0;
   const unsigned int zero = 0;
   if ((e = cudaMemcpyFromSymbol(&a, g_prefill_status, sizeof(a))) != cudaSuccess ||
       (e = cudaMemcpyFromSymbol(&b, g_decode_status, sizeof(b))) != cudaSuccess ||
-      (e = cudaMemcpyFromSymbol(&c, g_bwd_status, sizeof(c))) != cudaSuccess)
+      (e = cudaMemcpyFromSymbol(&c, g_bwd_status, sizeof(c))) != cudaSuccess ||
+      (e = cudaMemcpyFromSymbol(&t, g_selftest_status, sizeof(t))) != cudaSuccess)
     return cuda_fail(e, "reading the device status word");
-  if (a | b | c) {
+  if (a | b | c | t) {
     cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
+    cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(zero));
+    if ((a | c | t) == 0 && (b & ~kStatusDecodeBadPage) == 0)
+      return fail(B300ATTN_ERR_INVALID,
+                  "a paged decode met a block_table entry outside [0, num_pages); those keys "
+                  "were left out of the result");
     return fail(B300ATTN_ERR_TIMEOUT,
                 "a kernel gave up on a bounded wait (status bits prefill=0x%x decode=0x%x "
-                "backward=0x%x)",
-                a, b, c);
+                "backward=0x%x self-test=0x%x)",
+                a, b, c, t);
   }
   return B300ATTN_OK;
 }

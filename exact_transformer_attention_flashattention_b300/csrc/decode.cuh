@@ -26,6 +26,9 @@ namespace b300 {
 __device__ unsigned int g_decode_status;
 
 constexpr unsigned kStatusDecodeProducer = 8u, kStatusDecodeConsumer = 16u;
+// A paged decode met a block-table entry outside [0, num_pages): that stage
+// was treated as holding no keys (an input error, not a timeout).
+constexpr unsigned kStatusDecodeBadPage = 2048u;
 
 constexpr int kDecSub = 64;      // keys per ring stage
 constexpr int kDecCWarps = 4;    // consumer warps (16 keys of each stage each)
@@ -74,7 +77,11 @@ struct DecSmem {
   static constexpr int OFF_PROBS = OFF_SCORES + SCORES;
   static constexpr int OFF_ML = OFF_PROBS + PROBS;
   static constexpr int OFF_BARS = (OFF_ML + MERGE_ML + 15) & ~15;
-  static constexpr int BYTES = OFF_BARS + BARS + 128;  // + alignment slack
+  // ints: [0, STAGES) "stage holds keys" flags written by the producer,
+  // [STAGES] "a consumer wait ran out" flag
+  static constexpr int OFF_FLAGS = OFF_BARS + BARS;
+  static constexpr int FLAGS = (DecCfg<D>::STAGES + 1) * 4;
+  static constexpr int BYTES = OFF_FLAGS + FLAGS + 128;  // + alignment slack
 };
 
 // Eight bf16 (one 16-byte load) as four f32 pairs.
@@ -110,6 +117,8 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
   float* ml_sm = mm_sm + kDecCWarps * GT;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
   uint64_t* empty = full + STAGES;
+  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + L::OFF_FLAGS);
+  volatile int* failed = stage_ok + STAGES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -130,6 +139,7 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecCWarps);
     }
+    *failed = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -146,16 +156,26 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
             !mbar_wait(&empty[s], ((issued / STAGES) - 1) & 1, &g_decode_status,
                        kStatusDecodeProducer))
           break;
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         uint8_t* dst = smem + s * C::STAGE_BYTES;
         const int key = key0 + issued * kDecSub;
         int c2 = key, c3 = b;  // row and outer coordinate of the [.., rows, Hkv, D] view
+        bool page_ok = true;
         if (p.block_table) {
           c2 = key % p.page_size;
           c3 = p.block_table[static_cast<size_t>(b) * p.pages_per_seq + key / p.page_size];
+          page_ok = c3 >= 0 && c3 < p.num_pages;
         }
-        tma_load_4d(dst, &tm_k, &full[s], 0, hkv, c2, c3);
-        tma_load_4d(dst + C::HALF_BYTES, &tm_v, &full[s], 0, hkv, c2, c3);
+        // the flag is published by the arrive below (release) and read after
+        // the consumers' wait on it (acquire)
+        stage_ok[s] = page_ok ? 1 : 0;
+        if (page_ok) {
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_4d(dst, &tm_k, &full[s], 0, hkv, c2, c3);
+          tma_load_4d(dst + C::HALF_BYTES, &tm_v, &full[s], 0, hkv, c2, c3);
+        } else {
+          atomicOr(&g_decode_status, kStatusDecodeBadPage);
+          mbar_arrive(&full[s]);  // no copy: the stage counts as holding no keys
+        }
       }
       for (int u = max(0, issued - STAGES); u < issued; ++u)
         mbar_wait(&full[u % STAGES], (u / STAGES) & 1, &g_decode_status, kStatusDecodeProducer);
@@ -192,10 +212,13 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
   for (int sub = 0; sub < nsub; ++sub) {
     const int stage = sub % STAGES;
     bool ok = mbar_wait(&full[stage], (sub / STAGES) & 1, &g_decode_status, kStatusDecodeConsumer);
-    if (!__all_sync(0xffffffffu, ok)) break;
+    if (!__all_sync(0xffffffffu, ok)) {
+      *failed = 1;
+      break;
+    }
     const uint8_t* Ks = smem + stage * C::STAGE_BYTES;
     const uint8_t* Vs = Ks + C::HALF_BYTES;
-    const int nvalid = min(kDecSub, nkeys - sub * kDecSub);
+    const int nvalid = stage_ok[stage] ? min(kDecSub, nkeys - sub * kDecSub) : 0;
     const int wkey0 = warp * 16;  // this warp's 16 keys of the stage
 
     // ---- s = q . k for KPG keys x GT heads, partial over this lane's 8 elements
@@ -315,6 +338,20 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
 #pragma unroll
   for (int mask = GT; mask < 32; mask <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, mask);
   named_bar_sync(1, kDecCWarps * 32);  // every warp is done reading the ring
+  if (*failed) {
+    // A wait ran out: copies may still be landing in the ring, so it is not
+    // reused.  The split gets the identity partial (-inf, 0, 0).
+    for (int idx = threadIdx.x; idx < GT * D; idx += kDecCWarps * 32) {
+      const int g = idx / D, dd = idx % D;
+      const size_t prow = static_cast<size_t>(b) * p.Hq + hq0 + g;
+      p.part_o[(prow * p.S + split) * D + dd] = 0.f;
+      if (dd == 0) {
+        p.part_m[prow * p.S + split] = -INFINITY;
+        p.part_l[prow * p.S + split] = 0.f;
+      }
+    }
+    return;
+  }
   if (lane < LPK) {
 #pragma unroll
     for (int g = 0; g < GT; ++g)

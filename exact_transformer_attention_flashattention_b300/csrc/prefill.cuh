@@ -430,6 +430,26 @@ __global__ void __launch_bounds__(384, 1)
         const int sv = t % STAGES;
         if (!(ok = wait(&kv_full[sv], (t / STAGES) & 1))) break;
         tc_fence_after();
+        if constexpr (!FP8) {
+          // A tile that runs past the sequence's end holds the next
+          // sequence's rows (or TMA's zero fill) there.  Their scores are
+          // masked, so P = 0 for them, but 0 times a non-finite value is not
+          // 0: zero those V rows (whole 128-byte rows of every swizzle
+          // chunk) before the tensor core reads the stage.  FP8 needs no
+          // fix-up: its transposed V is zero past the sequence's end.
+          const int nv = it.n - j * BN;  // >= 1: every visited tile starts inside
+          if (nv < BN) {
+            uint8_t* vt = sRing + sv * C::TILE_BYTES;
+#pragma unroll 1
+            for (int cc = 0; cc < C::DCH; ++cc) {
+              uint4* z = reinterpret_cast<uint4*>(vt + cc * (BN * 128) + nv * 128);
+#pragma unroll 1
+              for (int e = lane; e < (BN - nv) * 8; e += 32) z[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // generic writes -> tensor-core operand
+            __syncwarp();
+          }
+        }
         const bool has_next = j < it.J1;
         const int sk = (t + 1) % STAGES;
         bool k_ready = false;

@@ -258,7 +258,8 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
  * loads the library holds that array until the process exits.  A call whose
  * partials would need more than that (attn_decode_workspace_size(B, Hq,
  * num_splits, d) > 40 MiB) returns B300ATTN_ERR_WORKSPACE with a message; e.g.
- * 1 sequence x 32 heads x 2048 splits x d=128 needs 33.5 MiB and fits.
+ * 1 sequence x 32 heads x 2048 splits x d=128 needs 32.5 MiB
+ * (34,078,720 bytes) and fits.
  *
  * The first call on a device looks up the scratch array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
@@ -287,8 +288,10 @@ int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* 
  *
  *   k_pages, v_pages  bf16 [num_pages, page_size, Hkv, d]
  *   block_table       int32 [B, pages_per_seq], device; entries for keys
- *                     < kv_len[b] must lie in [0, num_pages) (others are not read;
- *                     an out-of-range entry reads zeros, never out of bounds)
+ *                     < kv_len[b] must lie in [0, num_pages) (others are not read).
+ *                     The kernel checks each entry it reads: one outside that range
+ *                     is never dereferenced, its page counts as holding no keys, and
+ *                     the next attn_device_status returns B300ATTN_ERR_INVALID.
  *   kv_len            int32 [B], device; clamped to [0, pages_per_seq * page_size]
  *   page_size         a positive multiple of 64
  *   other arguments, the split, the workspace and the errors as for
@@ -339,12 +342,29 @@ int lse_tree_combine(const float* part_m, const float* part_l, const float* part
 
 /*
  * attn_device_status -- synchronises `stream`, then reads and clears this
- * library's device status word for the current device.  Returns
+ * library's device status words for the current device.  Returns
  * B300ATTN_ERR_TIMEOUT if any kernel gave up on a bounded wait since the last
  * call (the kernel then stopped early and its outputs are not valid),
- * B300ATTN_ERR_CUDA if the synchronisation failed, else B300ATTN_OK.
+ * B300ATTN_ERR_INVALID if the only event was a paged decode reading a
+ * block_table entry outside [0, num_pages), B300ATTN_ERR_CUDA if the
+ * synchronisation failed, else B300ATTN_OK.
  */
 int attn_device_status(cudaStream_t stream);
+
+/*
+ * attn_selftest_bounded_wait -- exercises the failure path that every
+ * pipeline wait of the kernels above shares.  One thread of a one-warp kernel
+ * waits on a shared-memory barrier that nothing ever arrives on, with no copy
+ * and no tensor-core work in flight; the wait gives up after `limit_ns`
+ * nanoseconds of %globaltimer, records its status bit and the kernel returns.
+ * The next attn_device_status(stream) then returns B300ATTN_ERR_TIMEOUT once
+ * and clears the bit, and the context stays usable.  (Not a step of the
+ * method: a test of the library's bounded waits, which exist so that a stuck
+ * pipeline stops instead of hanging the GPU.)
+ *   limit_ns  in [1000, 100000000] (1 us .. 100 ms), else B300ATTN_ERR_INVALID.
+ * Errors: INVALID, CUDA.
+ */
+int attn_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 /* Message describing the last non-OK status returned on this thread ("" if none). */
 const char* attn_last_error(void);

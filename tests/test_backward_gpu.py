@@ -73,3 +73,28 @@ def test_backward_is_deterministic(fa):
     b = fa.attn_bwd(q, k, v, O, L, dO, causal=True)
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_backward_full_size_sampled_heads(fa):
+    """The benchmarked backward launch (causal, B=4, H=16, N=4096, d=128,
+    heaviest-first order) at full size; the oracle recomputes two whole heads
+    (with Hq = Hkv a head's dQ, dK, dV depend on that head alone)."""
+    from exact_transformer_attention_flashattention_b300.inputs import WORKLOADS
+    w = WORKLOADS["causal_prefill_4k"]
+    q, k, v = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+    dO = torch.randn(w.B, w.N, w.Hq, w.d, generator=torch.Generator("cpu").manual_seed(11)
+                     ).bfloat16()
+    qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    O, L = fa.attn_fwd(qd, kd, vd, causal=True, scale=w.scale)
+    dq, dk, dv = fa.attn_bwd(qd, kd, vd, O, L, dOd, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    for b, h in [(0, 0), (w.B - 1, w.Hq - 1)]:
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        rq, rk, rv = oracle.attention_backward(q[sl], k[sl], v[sl], dO[sl], causal=True,
+                                               scale=w.scale)
+        _rel_close(dv[sl], rv, f"dV b={b} h={h}")
+        _rel_close(dk[sl], rk, f"dK b={b} h={h}")
+        _rel_close(dq[sl], rq, f"dQ b={b} h={h}")
