@@ -40,6 +40,7 @@ METRIC = "prefill attn TFLOP/s & decode KV GB/s on 1 B300, as % of roofline"
 PKG = "exact_transformer_attention_flashattention_b300"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 NAMEPLATE_HBM_GBS = 8000.0
+PLAIN_PAUSE_S = 1.5  # idle seconds before the plain-launch timing (clock recovery)
 
 
 def parse_args():
@@ -57,6 +58,8 @@ def parse_args():
                          "(a small command for kernel profiles; not the benchmark line)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--extra-cpu-budget", type=float, default=4.0,
+                    help="seconds of oracle work for each sub-workload's cpu_baseline")
     return ap.parse_args()
 
 
@@ -279,6 +282,17 @@ class ClockSampler:
     def window(self, t0, t1):
         self.t0, self.t1 = t0, t1
 
+    def stats(self, t0, t1):
+        """Median SM clock and the throttle reasons seen between t0 and t1."""
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "samples": 0, "reasons": []}
+        bits = 0
+        for s in inside:
+            bits |= s[2]
+        return {"sm_mhz": float(statistics.median(s[1] for s in inside)), "samples": len(inside),
+                "reasons": [n for n, bit in self.REASONS.items() if bits & bit and n != "gpu_idle"]}
+
     def __enter__(self):
         if self.ok:
             self._stop = threading.Event()
@@ -357,8 +371,13 @@ def time_launches(fn, steps: int, warmup: int, dist: Dist, clocks=None, graph: b
         clocks.window(t0, t1)
     dist.barrier()
     LAST_TIMING.clear()
-    LAST_TIMING.update({"mode": mode, "host_enqueue_ms_per_call": round((t_enq - t0) / steps * 1e3, 4)})
+    LAST_TIMING.update({"mode": mode, "host_enqueue_ms_per_call": round((t_enq - t0) / steps * 1e3, 4),
+                        "_t0": t0, "_t1": t1})
     return dist.max(start.elapsed_time(end) / steps)
+
+
+def public_timing(t: dict) -> dict:
+    return {k: v for k, v in t.items() if not k.startswith("_")}
 
 
 def whole_job_rate(units_per_rank: float, world: int, ms_max: float, scale: float) -> float:
@@ -395,15 +414,28 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
     def step():
         fa.attn_fwd(q, k, v, causal=w.causal, window=w.window, scale=w.scale, out=o, lse=lse)
 
-    if clocks is not None:
-        with clocks:
-            ms = time_launches(step, steps, warmup, dist, clocks)
-    else:
-        ms = time_launches(step, steps, warmup, dist)
-    timing = dict(LAST_TIMING)
-    ms_plain = time_launches(step, steps, warmup, dist, graph=False)
+    own = clocks is None
+    if own:
+        clocks = ClockSampler(torch.cuda.current_device())
+    with clocks:
+        ms = time_launches(step, steps, warmup, dist, clocks)
+        timing = dict(LAST_TIMING)
+        graph_clk = clocks.stats(timing["_t0"], timing["_t1"])
+        # Plain launches, after an idle pause: a long burst of this kernel
+        # draws enough power that the SM clock steps down within tens of ms,
+        # so whichever of two back-to-back timings runs second would see a
+        # lower clock.  The pause lets the clock return before the second one.
+        time.sleep(PLAIN_PAUSE_S)
+        ms_plain = time_launches(step, steps, warmup, dist, graph=False)
+        plain_clk = clocks.stats(LAST_TIMING["_t0"], LAST_TIMING["_t1"])
+    if not own:
+        clocks.window(timing["_t0"], timing["_t1"])
+    timing = public_timing(timing)
+    timing["graph_clock_mhz"] = graph_clk["sm_mhz"]
     timing["plain_launch_ms"] = round(ms_plain, 5)
     timing["plain_host_enqueue_ms_per_call"] = LAST_TIMING["host_enqueue_ms_per_call"]
+    timing["plain_clock_mhz"] = plain_clk["sm_mhz"]
+    timing["plain_reasons"] = plain_clk["reasons"]
     assert fa.device_status() == 0, fa.last_error()
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -416,7 +448,7 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             "launches_per_step": 1, "timing": timing}
 
 
-def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
+def bench_backward(w, steps, warmup, dist, peaks, peak_kind, cpu_budget=0.0):
     """The backward of the prefill workload (dQ, dK, dV from O, LSE and a random
     dO).  Algorithmic work: five products of 2*d flops per unmasked pair (S, dP,
     dV, dK, dQ), 2.5 times the forward's; the kernels recompute S and dP once
@@ -437,7 +469,7 @@ def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
                     dq=dq, dk=dk, dv=dv, workspace=ws)
 
     ms = time_launches(step, steps, warmup, dist)
-    timing = dict(LAST_TIMING)
+    timing = public_timing(LAST_TIMING)
     assert fa.device_status() == 0, fa.last_error()
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -446,9 +478,25 @@ def bench_backward(w, steps, warmup, dist, peaks, peak_kind):
     # traffic of the three launches is not one kernel's; the dK/dV kernel's own
     # DRAM bytes (ncu) are reported beside the roofline
     rf["traffic_bwd_dkdv_kernel"] = stored_traffic("bwd_dkdv_kernel", w.name + "_backward")
-    return {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
-            "launches_per_call": 3, "timing": timing,
-            "config": dict(workload_config(w), workload=w.name + "_backward")}
+    res = {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
+           "launches_per_call": 3, "timing": timing,
+           "config": dict(workload_config(w), workload=w.name + "_backward")}
+    if cpu_budget > 0 and dist.rank == 0:
+        import oracle
+        from exact_transformer_attention_flashattention_b300.inputs import prefill_inputs
+        qh, kh, vh = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+        dOh = dO.cpu()
+        pairs = [(i % w.B, (i * 7) % w.Hq) for i in range(w.B * w.Hq)]
+
+        def run(i):  # Hq == Hkv: one head's gradients need that head alone
+            b, h = pairs[i]
+            sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+            oracle.attention_backward(qh[sl], kh[sl], vh[sl], dOh[sl], causal=w.causal,
+                                      window=w.window, scale=w.scale)
+        res["cpu_baseline"] = cpu_baseline_heads(
+            w.name + "_backward", flops / (w.B * w.Hq), run, len(pairs), cpu_budget,
+            "dQ, dK, dV of whole heads, float64 NumPy")
+    return res
 
 
 def bench_fp8(w, steps, warmup, dist, peaks, peak_kind):
@@ -473,7 +521,7 @@ def bench_fp8(w, steps, warmup, dist, peaks, peak_kind):
         fa.attn_fp8_quantize(q, k, v, out=qz, workspace=ws)
 
     ms = time_launches(attn, steps, warmup, dist)
-    timing = dict(LAST_TIMING)
+    timing = public_timing(LAST_TIMING)
     ms_q = time_launches(quant, steps, warmup, dist)
     assert fa.device_status() == 0, fa.last_error()
     tflops = flops / (ms * 1e-3) / 1e12
@@ -491,12 +539,134 @@ def bench_fp8(w, steps, warmup, dist, peaks, peak_kind):
             "config": dict(workload_config(w), workload=w.name + "_fp8")}
 
 
-def decode_case(w, dev):
+def prefill_extra(w, steps, warmup, dist, peaks, peak_kind, cpu_budget=0.0):
+    """A prefill workload as a sub-object: TFLOP/s with its roofline, timing,
+    and the oracle on whole heads of the same inputs (the band form for a
+    non-causal window, whose masked keys carry exactly zero weight)."""
+    r = bench_prefill(w, steps, warmup, dist, peaks, peak_kind)
+    out = {"value": round(r["tflops"], 2), "unit": "TFLOP/s", "ms_per_call": r["ms"],
+           "us_per_call": round(r["ms"] * 1e3, 2), "roofline": r["roofline"],
+           "timing": r["timing"], "config": workload_config(w)}
+    if cpu_budget > 0 and dist.rank == 0:
+        import oracle
+        from exact_transformer_attention_flashattention_b300.inputs import (prefill_flops,
+                                                                            prefill_inputs)
+        q, k, v = prefill_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed)
+        pairs = [(i % w.B, (i * 7) % w.Hq) for i in range(w.B * w.Hq)]
+        per_head = prefill_flops(1, 1, w.N, w.d, w.causal, w.window)
+        if w.window >= 0 and not w.causal:
+            run = lambda i: oracle.attention_band(q, k, v, w.window, scale=w.scale,
+                                                  heads=[pairs[i]])
+            what = "band form over every query row, float64 NumPy"
+        else:
+            run = lambda i: oracle.attention_rows(q, k, v, *pairs[i], list(range(w.N)),
+                                                  causal=w.causal, window=w.window,
+                                                  scale=w.scale)
+            what = "every query row, float64 NumPy"
+        out["cpu_baseline"] = cpu_baseline_heads(w.name, per_head, run, len(pairs), cpu_budget,
+                                                 what)
+    return out
+
+
+def bench_paged(w, steps, warmup, dist, peaks, peak_kind, page_size=256):
+    """The prefill workload with K and V in a shuffled page pool (block table),
+    as an inference server keeps its cache."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import prefill_flops
+    q, k, v, o, lse = prefill_case(w, "cuda")
+    pps = (w.N + page_size - 1) // page_size
+    P = w.B * pps
+    perm = torch.randperm(P, generator=torch.Generator("cpu").manual_seed(w.seed + 7))
+    table = perm.view(w.B, pps).to(torch.int32).cuda()
+    k_pages = torch.empty(P, page_size, w.Hkv, w.d, dtype=torch.bfloat16, device="cuda")
+    v_pages = torch.empty_like(k_pages)
+    k_pages[table.long()] = k.view(w.B, pps, page_size, w.Hkv, w.d)
+    v_pages[table.long()] = v.view(w.B, pps, page_size, w.Hkv, w.d)
+    del k, v
+    flops = prefill_flops(w.B, w.Hq, w.N, w.d, w.causal, w.window)
+
+    def step():
+        fa.attn_fwd_paged(q, k_pages, v_pages, table, causal=w.causal, window=w.window,
+                          scale=w.scale, out=o, lse=lse)
+
+    ms = time_launches(step, steps, warmup, dist)
+    timing = public_timing(LAST_TIMING)
+    assert fa.device_status() == 0, fa.last_error()
+    tflops = flops / (ms * 1e-3) / 1e12
+    rf = roofline(tflops, peaks["bf16_tflops"], "TFLOP/s", "tensor", None, flops, "FLOP")
+    rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
+            "launches_per_call": 1, "timing": timing,
+            "config": dict(workload_config(w), workload=w.name + "_paged", page_size=page_size,
+                           pages="shuffled pool, one block-table row per sequence")}
+
+
+def bench_alternating(lw, steps, warmup, dist, peaks, peak_kind, cpu_budget=0.0):
+    """A stack of layers alternating global and local attention (layer l global
+    when l % 3 == 0), two calls per group of three layers."""
+    import torch
+    from exact_transformer_attention_flashattention_b300 import alternating
+    from exact_transformer_attention_flashattention_b300 import binding as fa
+    from exact_transformer_attention_flashattention_b300.inputs import (layer_stack_inputs,
+                                                                        prefill_flops)
+    host = layer_stack_inputs(lw.L, lw.B, lw.Hq, lw.Hkv, lw.N, lw.d, lw.seed)
+    q, k, v = (t.cuda() for t in host)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(lw.L, lw.B, lw.Hq, lw.N, dtype=torch.float32, device="cuda")
+    groups = alternating.layer_groups(lw.L, lw.global_every)
+    f_glob = prefill_flops(lw.B, lw.Hq, lw.N, lw.d, False, -1)
+    f_loc = prefill_flops(lw.B, lw.Hq, lw.N, lw.d, False, lw.local_window)
+    n_glob = len(groups)
+    flops = n_glob * f_glob + (lw.L - n_glob) * f_loc
+
+    def step():
+        alternating.alternating_attention(q, k, v, lw.global_every, lw.local_window,
+                                          scale=lw.scale, out=o, lse=lse)
+
+    ms = time_launches(step, steps, warmup, dist)
+    timing = public_timing(LAST_TIMING)
+    assert fa.device_status() == 0, fa.last_error()
+    tflops = flops / (ms * 1e-3) / 1e12
+    rf = roofline(tflops, peaks["bf16_tflops"], "TFLOP/s", "tensor", None, flops, "FLOP")
+    rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
+    out = {"value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": ms, "roofline": rf,
+           "launches_per_call": 2 * n_glob - sum(1 for _, a, e in groups if e == a),
+           "timing": timing,
+           "config": {"workload": lw.name, "layers": lw.L, "B": lw.B, "Hq": lw.Hq, "Hkv": lw.Hkv,
+                      "N": lw.N, "d": lw.d, "global_every": lw.global_every,
+                      "local_window": f"|i-j| <= {lw.local_window}", "causal": False,
+                      "scale": "1/sqrt(d)", "inputs": "bf16 i.i.d. N(0,1), seeded",
+                      "l2": "inputs larger than L2; no flush"}}
+    if cpu_budget > 0 and dist.rank == 0:
+        import oracle
+        qh, kh, vh = host
+        G = lw.global_every
+
+        def run(i):  # alternate a global head and a local head of the first group
+            layer = 0 if i % 2 == 0 else 1
+            b, h = (i // 2) % lw.B, (i // 2) % lw.Hq
+            if layer == 0:
+                oracle.attention_rows(qh[0], kh[0], vh[0], b, h, list(range(lw.N)),
+                                      scale=lw.scale)
+            else:
+                oracle.attention_band(qh[1], kh[1], vh[1], lw.local_window, scale=lw.scale,
+                                      heads=[(b, h)])
+        per_pair = (prefill_flops(1, 1, lw.N, lw.d, False, -1) +
+                    prefill_flops(1, 1, lw.N, lw.d, False, lw.local_window)) / 2
+        out["cpu_baseline"] = cpu_baseline_heads(
+            lw.name, per_pair, run, lw.L * lw.B * lw.Hq, cpu_budget,
+            "global and local heads alternately (local in band form), float64 NumPy")
+    return out
+
+
+def decode_case(w, dev, host=None):
     import torch
     from exact_transformer_attention_flashattention_b300 import binding as fa
     from exact_transformer_attention_flashattention_b300.inputs import decode_inputs
-    q, kc, vc, kv_len = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo,
-                                      w.kv_len_hi)
+    if host is None:
+        host = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo, w.kv_len_hi)
+    q, kc, vc, kv_len = host
     ws = torch.empty(fa.attn_decode_workspace_size(w.B, w.Hq, w.num_splits, w.d),
                      dtype=torch.uint8, device=dev)
     o = torch.empty(w.B, w.Hq, w.d, dtype=torch.bfloat16, device=dev)
@@ -504,10 +674,14 @@ def decode_case(w, dev):
     return q.to(dev), kc.to(dev), vc.to(dev), kv_len, kv_len.to(dev), ws, o, lse
 
 
-def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
+def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None, cpu_budget=0.0):
     from exact_transformer_attention_flashattention_b300 import binding as fa
-    from exact_transformer_attention_flashattention_b300.inputs import decode_kv_bytes
-    q, kc, vc, kv_len_host, kv_len, ws, o, lse = decode_case(w, "cuda")
+    from exact_transformer_attention_flashattention_b300.inputs import (decode_inputs,
+                                                                        decode_kv_bytes)
+    host = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo, w.kv_len_hi)
+    base = cpu_baseline_decode(w, cpu_budget, host) if cpu_budget > 0 and dist.rank == 0 else None
+    q, kc, vc, kv_len_host, kv_len, ws, o, lse = decode_case(w, "cuda", host)
+    del host
     kv_bytes = decode_kv_bytes(kv_len_host, w.Hkv, w.d)
     m, l, po = fa.split_partials_view(ws, w.B, w.Hq, w.num_splits, w.d)
 
@@ -526,7 +700,7 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
             ms_full = time_launches(full, steps, warmup, dist, clocks)
     else:
         ms_full = time_launches(full, steps, warmup, dist)
-    timing = dict(LAST_TIMING)
+    timing = public_timing(LAST_TIMING)
     ms_part = time_launches(partials, steps, warmup, dist)
     ms_comb = time_launches(combine, steps, warmup, dist)
     assert fa.device_status() == 0, fa.last_error()
@@ -537,15 +711,15 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
     rf["kernel"] = "decode_partial_kernel"
     rf["peak_kind"] = f"{peak_kind} HBM copy"
     rf["frac_of_nameplate_8tbs"] = round(part_gbs / NAMEPLATE_HBM_GBS, 4)
-    return {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": ms_full,
-            "kv_bytes": kv_bytes, "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
-            "frac_of_nameplate_8tbs": round(gbs / NAMEPLATE_HBM_GBS, 4),
-            "kernels": {"decode_partial_kernel_ms": ms_part, "lse_combine_kernel_ms": ms_comb},
-            "launches_per_call": 2, "roofline": rf, "timing": timing,
-            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lmax": w.N, "d": w.d,
-                       "num_splits": w.num_splits,
-                       "kv_len": "uniform [%d, %d]" % (w.kv_len_lo, w.kv_len_hi)
-                       if w.kv_len_lo else "full"}}
+    res = {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": ms_full,
+           "kv_bytes": kv_bytes, "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+           "frac_of_nameplate_8tbs": round(gbs / NAMEPLATE_HBM_GBS, 4),
+           "kernels": {"decode_partial_kernel_ms": ms_part, "lse_combine_kernel_ms": ms_comb},
+           "launches_per_call": 2, "roofline": rf, "timing": timing,
+           "config": decode_config(w)}
+    if base is not None:
+        res["cpu_baseline"] = base
+    return res
 
 
 def e2e_prefill(w, steps, dist):
@@ -656,13 +830,14 @@ def cpu_baseline(w, budget_s: float):
             "host_cores_available": len(os.sched_getaffinity(0))}
 
 
-def cpu_baseline_decode(w, budget_s: float):
-    """The oracle decode on whole (sequence, query head) rows until about
-    `budget_s` seconds of work; GB/s of K/V rows it read."""
+def cpu_baseline_decode(w, budget_s: float, inputs=None):
+    """The oracle decode on whole (sequence, kv head) groups (every query head
+    of the group) until about `budget_s` seconds of work; GB/s of K/V rows read."""
     import oracle
     from exact_transformer_attention_flashattention_b300.inputs import decode_inputs
-    q, kc, vc, kv_len = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo,
-                                      w.kv_len_hi)
+    if inputs is None:
+        inputs = decode_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.kv_len_lo, w.kv_len_hi)
+    q, kc, vc, kv_len = inputs
     G = w.Hq // w.Hkv
     secs = nbytes = 0.0
     done = 0
@@ -685,6 +860,23 @@ def cpu_baseline_decode(w, budget_s: float):
             "host_cores_available": len(os.sched_getaffinity(0))}
 
 
+def cpu_baseline_heads(name, flops_per_head, run_head, n_heads, budget_s: float, what: str):
+    """The oracle on whole (batch, head) pairs until about `budget_s` seconds;
+    `run_head(i)` computes pair i, `flops_per_head` is its algorithmic work."""
+    secs = flops = 0.0
+    done = 0
+    while done < n_heads and (done == 0 or secs < budget_s):
+        t0 = time.perf_counter()
+        run_head(done)
+        secs += time.perf_counter() - t0
+        flops += flops_per_head
+        done += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": blas_threads() or len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{done} of {n_heads} (batch, head) pairs of {name}, {what} ({secs:.1f} s)",
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
 def run_reference(args, w, dist):
     """--impl reference: the oracle timed on bounded samples of the workload."""
     if dist.rank != 0:
@@ -696,7 +888,8 @@ def run_reference(args, w, dist):
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": decode_config(w), "cpu_baseline": r,
+                "config": dict(decode_config(w), parallelism=parallelism(dist)),
+                "cpu_baseline": r,
                 "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -720,7 +913,7 @@ def run_reference(args, w, dist):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
+            "config": dict(workload_config(w), parallelism=parallelism(dist)),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle",
                              "sample": f"per step: the last {rows} query rows of one (batch, "
@@ -730,6 +923,30 @@ def run_reference(args, w, dist):
     print(json.dumps(line), flush=True)
 
 
+def summary(line):
+    """One compact entry per workload of the line (value, unit, roofline
+    fraction, the oracle's CPU rate), printed last so that it survives in the
+    tail of the output."""
+    def entry(o):
+        rf = o.get("roofline", {})
+        e = {"value": o.get("value"), "unit": o.get("unit"), "frac": rf.get("frac"),
+             "of": rf.get("unit")}
+        if "us_per_call" in o:
+            e["us"] = o["us_per_call"]
+        if "frac_of_hbm_peak" in o:
+            e["whole_call_frac"] = o["frac_of_hbm_peak"]
+        if "cpu_baseline" in o:
+            e["cpu"] = o["cpu_baseline"]["value"]
+        return e
+    out = {line["config"]["workload"]: entry(line)}
+    if "timing" in line and "plain_launch_ms" in line["timing"]:
+        out[line["config"]["workload"]]["plain_launch_ms"] = line["timing"]["plain_launch_ms"]
+        out[line["config"]["workload"]]["ms"] = line["ms_per_step"]
+    for name, o in line.get("extra", {}).items():
+        out[name] = entry(o)
+    return out
+
+
 def workload_config(w):
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
            "causal": w.causal, "window": w.window, "scale": "1/sqrt(d)",
@@ -737,6 +954,10 @@ def workload_config(w):
     qkv = w.B * w.N * (w.Hq + 2 * w.Hkv) * w.d * 2
     cfg["l2"] = f"inputs larger than L2 ({qkv / 2**20:.0f} MiB of Q/K/V vs 126 MB); no flush"
     return cfg
+
+
+def parallelism(dist):
+    return f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
 
 
 def decode_config(w):
@@ -792,36 +1013,38 @@ def main():
         line["kernels"] = main_res["kernels"]
     if "timing" in main_res:
         line["timing"] = main_res["timing"]
-    line["config"]["parallelism"] = f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
+    line["config"]["parallelism"] = parallelism(dist)
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 10))
         line["e2e"] = e2e_prefill(w, e2e_steps, dist) if w.kind == "prefill" else \
             e2e_decode(w, e2e_steps, dist)
-    if not args.no_extra:
-        extra = {}
-        for name in ("decode_1m", "gqa_decode_batch32"):
-            if name == w.name:
-                continue
-            extra[name] = bench_decode(WORKLOADS[name], max(3, min(args.steps, 50)),
-                                       max(3, args.warmup), dist, peaks, peak_kind)
-        if w.name == "causal_prefill_4k":
-            extra["causal_prefill_4k_backward"] = bench_backward(
-                w, max(3, min(args.steps, 50)), max(3, args.warmup), dist, peaks, peak_kind)
-            extra["causal_prefill_4k_fp8"] = bench_fp8(
-                w, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks, peak_kind)
-        for name in ("window_encoder_8k", "causal_prefill_4k"):
-            if name == w.name:
-                continue
-            wn = WORKLOADS[name]
-            r = bench_prefill(wn, max(3, min(args.steps, 100)), max(3, args.warmup), dist, peaks,
-                              peak_kind)
-            extra[name] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
-                           "ms_per_call": r["ms"], "roofline": r["roofline"],
-                           "timing": r["timing"], "config": workload_config(wn)}
-        line["extra"] = extra
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget) if w.kind == "prefill" else \
             cpu_baseline_decode(w, args.cpu_budget)
+    if not args.no_extra:
+        from exact_transformer_attention_flashattention_b300.inputs import LAYER_WORKLOADS
+        budget = 0.0 if args.no_cpu_baseline else args.extra_cpu_budget
+        n_ex, w_ex = max(3, min(args.steps, 100)), max(3, args.warmup)
+        extra = {}
+        # prefill legs first; the decode legs go last in the line
+        for name in ("tiny_noncausal", "window_encoder_8k", "causal_prefill_4k"):
+            if name != w.name:
+                extra[name] = prefill_extra(WORKLOADS[name], n_ex, w_ex, dist, peaks, peak_kind,
+                                            budget)
+        if w.name == "causal_prefill_4k":
+            extra["causal_prefill_4k_backward"] = bench_backward(
+                w, max(3, min(args.steps, 50)), w_ex, dist, peaks, peak_kind, budget)
+            extra["causal_prefill_4k_fp8"] = bench_fp8(w, n_ex, w_ex, dist, peaks, peak_kind)
+            extra["causal_prefill_4k_paged"] = bench_paged(w, n_ex, w_ex, dist, peaks, peak_kind)
+        lw = LAYER_WORKLOADS["modernbert_alternating_8k"]
+        extra[lw.name] = bench_alternating(lw, max(3, min(args.steps, 30)), w_ex, dist, peaks,
+                                           peak_kind, budget)
+        for name in ("gqa_decode_batch32", "decode_1m"):
+            if name != w.name:
+                extra[name] = bench_decode(WORKLOADS[name], max(3, min(args.steps, 50)), w_ex,
+                                           dist, peaks, peak_kind, cpu_budget=budget)
+        line["extra"] = extra
+        line["summary"] = summary(line)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()

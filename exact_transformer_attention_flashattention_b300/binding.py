@@ -26,6 +26,8 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]),
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P,
                              _I]),
+    "attn_fwd_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                            _F, _P, _I]),
     "attn_bwd_workspace_size": (_SZ, [_I, _I, _I]),
     "attn_fp8_padded_len": (_I, [_I]),
     "attn_fp8_workspace_size": (_SZ, [_I, _I, _I]),
@@ -153,6 +155,34 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, 
     _check(_lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
                                 S, T, int(max_seqlen), Hq, Hkv, d, int(bool(causal)), int(window),
                                 float(scale), _stream(stream), _odtype(out.dtype)))
+    return out, lse
+
+
+def attn_fwd_paged(q, k_pages, v_pages, block_table, causal: bool = False, window: int = -1,
+                   scale: float | None = None, out=None, lse=None, out_dtype=torch.bfloat16,
+                   stream=None):
+    """Prefill with K/V in a page pool.  q [B,N,Hq,d] bf16; pages [P, page_size, Hkv, d]
+    bf16; block_table int32 [B, pages_per_seq] -> (O [B,N,Hq,d], LSE [B,Hq,N])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    B, N, Hq, d = q.shape
+    P, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if k_pages.shape != (P, page_size, Hkv, d) or v_pages.shape != k_pages.shape:
+        raise ValueError("page pool shapes do not match q")
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _check(_lib.attn_fwd_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                               _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, page_size, P,
+                               block_table.shape[1], int(bool(causal)), int(window), float(scale),
+                               _stream(stream), _odtype(out.dtype)))
     return out, lse
 
 

@@ -164,6 +164,34 @@ int launch_prefill(const void* q, const void* k, const void* v, const PrefillPar
   return B300ATTN_OK;
 }
 
+// Paged prefill: q dense [B*N, Hq, D] (3-D map, 128-row boxes); K and V
+// pools [num_pages, page_size, Hkv, D] (4-D maps, 64-row boxes).
+template <int D>
+int launch_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                         const PrefillParams& p, cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map_3d(&tq, q, D, p.Hq, p.total_rows, 64, 1, C::BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tk, k_pages, D, p.Hkv, p.page_size, p.num_pages, 64, 1, 64, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k_pages")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_4d(&tv, v_pages, D, p.Hkv, p.page_size, p.num_pages, 64, 1, 64, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v_pages")) != B300ATTN_OK)
+    return rc;
+  auto kernel = prefill_kernel<D, false, false, true>;
+  if ((rc = set_smem(kernel, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != B300ATTN_OK) return rc;
+  const int grid = std::min(p.n_items, sms);
+  kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  return B300ATTN_OK;
+}
+
 // FP8 prefill (d = 128, dense): q8 [B*N, Hq, 128] and k8 [B*N, Hkv, 128]
 // e4m3 seen as [rows, heads, d] with one 128-byte box per row; v8t
 // [B*Hkv, 128, Np] with boxes of 128 keys x all of d.
@@ -454,6 +482,66 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.n_items = static_cast<int>(items);
   return d == 128 ? launch_prefill<128>(q, k, v, p, p.n_items, stream)
                   : launch_prefill<64>(q, k, v, p, p.n_items, stream);
+}
+
+int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                   const int* block_table, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                   int d, int page_size, int num_pages, int pages_per_seq, int causal,
+                   int window, float scale, cudaStream_t stream, int o_dtype) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 0 || d < 0 || page_size < 0 || num_pages < 0 ||
+      pages_per_seq < 0)
+    return fail(B300ATTN_ERR_INVALID, "negative size");
+  if (B == 0 || N == 0 || Hq == 0) return B300ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(B300ATTN_ERR_INVALID, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  int rc = check_common(d, o_dtype);
+  if (rc != B300ATTN_OK) return rc;
+  if (page_size < 64 || page_size % 64 != 0)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "page_size=%d must be a positive multiple of 64",
+                page_size);
+  if (num_pages < 1 || pages_per_seq < 1)
+    return fail(B300ATTN_ERR_INVALID, "num_pages and pages_per_seq must be >= 1");
+  if (static_cast<long long>(pages_per_seq) * page_size < N)
+    return fail(B300ATTN_ERR_INVALID, "pages_per_seq * page_size = %lld < N = %d",
+                static_cast<long long>(pages_per_seq) * page_size, N);
+  if (!q || !k_pages || !v_pages || !block_table || !o || !lse)
+    return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+      !aligned16(lse))
+    return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+    return fail(B300ATTN_ERR_INVALID, "block_table must be 4-byte aligned");
+  if (causal != 0 && causal != 1) return fail(B300ATTN_ERR_INVALID, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(B300ATTN_ERR_INVALID, "scale must be finite and >= 0 (got %g)",
+                static_cast<double>(scale));
+  if (static_cast<long long>(B) * N > 0x7fffffffLL)
+    return fail(B300ATTN_ERR_UNSUPPORTED, "B*N=%lld rows exceed 2^31-1",
+                static_cast<long long>(B) * N);
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = nullptr;
+  p.num_seqs = B;
+  p.total_rows = B * N;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.window = window < 0 ? -1 : window;
+  p.o_f32 = o_dtype == B300ATTN_F32;
+  p.nqb = (N + 255) / 256;
+  p.scale_log2 = std::fmax(scale * kLog2e, 1e-30f);
+  p.block_table = block_table;
+  p.page_size = page_size;
+  p.pages_per_seq = pages_per_seq;
+  p.num_pages = num_pages;
+  const long long items = static_cast<long long>(p.nqb) * Hq * B;
+  if (items > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
+  p.n_items = static_cast<int>(items);
+  return d == 128 ? launch_prefill_paged<128>(q, k_pages, v_pages, p, stream)
+                  : launch_prefill_paged<64>(q, k_pages, v_pages, p, stream);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -818,10 +906,11 @@ int attn_device_status(cudaStream_t stream) {
     cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(zero));
-    if ((a | c | t) == 0 && (b & ~kStatusDecodeBadPage) == 0)
+    if ((a & ~kStatusPrefillBadPage) == 0 && (c | t) == 0 && (b & ~kStatusDecodeBadPage) == 0)
       return fail(B300ATTN_ERR_INVALID,
-                  "a paged decode met a block_table entry outside [0, num_pages); those keys "
-                  "were left out of the result");
+                  "a paged call met a block_table entry outside [0, num_pages) (prefill bits "
+                  "0x%x, decode bits 0x%x); those keys were left out of the result",
+                  a, b);
     return fail(B300ATTN_ERR_TIMEOUT,
                 "a kernel gave up on a bounded wait (status bits prefill=0x%x decode=0x%x "
                 "backward=0x%x self-test=0x%x)",

@@ -45,6 +45,9 @@ namespace b300 {
 __device__ unsigned int g_prefill_status;  // OR of kStatus* bits (bounded waits that ran out)
 
 constexpr unsigned kStatusProducer = 1u, kStatusMma = 2u, kStatusSoftmax = 4u;
+// A paged prefill met a block-table entry outside [0, num_pages): the keys of
+// that page were read as zeros (an input error, not a timeout).
+constexpr unsigned kStatusPrefillBadPage = 4096u;
 
 // Maximum number of sequences of one variable-length launch (the per-CTA item
 // table lives in shared memory).
@@ -72,6 +75,12 @@ struct PrefillParams {
   const int* k_exp;  // [B, Hkv, nt]
   const int* v_exp;  // [B, Hkv]
   int nt;            // 128-row tiles per sequence
+  // Paged K/V (dense layout of q): K, V are [num_pages, page_size, Hkv, d] and
+  // key j of sequence b is row j % page_size of page
+  // block_table[b * pages_per_seq + j / page_size]; page_size is a multiple
+  // of 64, the rows of one TMA box.
+  const int* block_table;
+  int page_size, pages_per_seq, num_pages;
 };
 
 template <int D, bool FP8 = false>
@@ -191,11 +200,16 @@ __device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p,
 // scale * 2^-(e_Q + e_K) of the tile pair, writes P rounded to e4m3 into a
 // swizzled shared-memory tile (the A operand of PV), and the epilogue divides
 // by l and by 2^e_V.  The lazy rescale keeps P <= 2^8 < 448, inside e4m3.
-template <int D, bool VARLEN, bool FP8 = false>
+//
+// PAGED selects K and V gathered from a page pool through a block table
+// (dense layout of q, bf16): each 128-key tile is two 64-row TMA boxes, each
+// from the page that holds its keys.
+template <int D, bool VARLEN, bool FP8 = false, bool PAGED = false>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   static_assert(!FP8 || (D == 128 && !VARLEN), "FP8: dense layout, d = 128");
+  static_assert(!PAGED || (!FP8 && !VARLEN), "paged K/V: dense bf16 layout");
   using C = PrefillCfg<D, FP8>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
@@ -336,6 +350,28 @@ __global__ void __launch_bounds__(384, 1)
             else
               tma_load_3d(sRing + s * C::TILE_BYTES, &tm_k, &kv_full[s], 0, it.hk,
                           it.base + j * BN);
+          } else if constexpr (PAGED) {
+            // two 64-key boxes, each from its own page; keys past the
+            // sequence's end use page coordinate num_pages, which TMA fills
+            // with zeros (the block table is not read there)
+            const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
+            for (int hh = 0; hh < 2; ++hh) {
+              const int kr = j * BN + hh * 64;
+              int page = p.num_pages, prow = 0;
+              if (kr < it.n) {
+                const int e =
+                    p.block_table[static_cast<size_t>(it.b) * p.pages_per_seq + kr / p.page_size];
+                if (e >= 0 && e < p.num_pages) {
+                  page = e;
+                  prow = kr % p.page_size;
+                } else {
+                  atomicOr(&g_prefill_status, kStatusPrefillBadPage);
+                }
+              }
+              for (int cc = 0; cc < C::DCH; ++cc)
+                tma_load_4d(sRing + s * C::TILE_BYTES + cc * (BN * 128) + hh * 64 * 128, tm,
+                            &kv_full[s], cc * 64, it.hk, prow, page);
+            }
           } else {
             const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
             for (int cc = 0; cc < C::DCH; ++cc)

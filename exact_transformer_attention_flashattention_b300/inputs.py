@@ -25,6 +25,9 @@ import torch
 __all__ = [
     "Workload",
     "WORKLOADS",
+    "LayerStack",
+    "LAYER_WORKLOADS",
+    "layer_stack_inputs",
     "prefill_inputs",
     "decode_inputs",
     "prefill_flops",
@@ -75,6 +78,36 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class LayerStack:
+    """A stack of L attention layers whose global / local pattern alternates
+    (layer l global when l % global_every == 0, local window otherwise)."""
+
+    name: str
+    L: int
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    seed: int
+    global_every: int = 3
+    local_window: int = 64
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# ModernBERT-style encoder stack (12 heads of d=64, an 8192-token context):
+# two groups of one global and two local layers.  Seed 5 follows the five
+# workloads above.
+LAYER_WORKLOADS = {
+    "modernbert_alternating_8k": LayerStack("modernbert_alternating_8k", L=6, B=4, Hq=12, Hkv=12,
+                                            N=8192, d=64, seed=5),
+}
+
+
 def _randn_bf16(shape, g: torch.Generator) -> torch.Tensor:
     return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
 
@@ -85,6 +118,15 @@ def prefill_inputs(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int):
     q = _randn_bf16((B, N, Hq, d), g)
     k = _randn_bf16((B, N, Hkv, d), g)
     v = _randn_bf16((B, N, Hkv, d), g)
+    return q, k, v
+
+
+def layer_stack_inputs(L: int, B: int, Hq: int, Hkv: int, N: int, d: int, seed: int):
+    """q [L,B,N,Hq,d], k [L,B,N,Hkv,d], v [L,B,N,Hkv,d], bf16 on the CPU (layers stacked)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = _randn_bf16((L, B, N, Hq, d), g)
+    k = _randn_bf16((L, B, N, Hkv, d), g)
+    v = _randn_bf16((L, B, N, Hkv, d), g)
     return q, k, v
 
 

@@ -169,6 +169,31 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const int* q_e
                  int o_dtype);
 
 /*
+ * attn_fwd_paged -- attn_fwd with K and V kept in a paged pool, the layout an
+ * inference server keeps its KV cache in ("FlashAttention" learn page, "The
+ * future of FlashAttention": integration into inference servers, and variants
+ * for irregular attention).  Sequence b's key/value j is row j % page_size of
+ * page block_table[b * pages_per_seq + j / page_size]; each 128-key tile is
+ * gathered by two 64-row TMA copies.  Queries, masks, O and LSE are exactly
+ * those of attn_fwd with the gathered K and V.
+ *
+ *   q            bf16 [B, N, Hq, d]
+ *   k_pages, v_pages  bf16 [num_pages, page_size, Hkv, d]
+ *   block_table  int32 [B, pages_per_seq], device; entries for keys < N must
+ *                lie in [0, num_pages); entries past a sequence's N keys are
+ *                not read.  The kernel checks each entry it reads: one out of
+ *                range is never dereferenced, its keys read as zeros, and the
+ *                next attn_device_status returns B300ATTN_ERR_INVALID.
+ *   page_size    a positive multiple of 64;  pages_per_seq * page_size >= N
+ *   o, lse, causal, window, scale, o_dtype, stream  as for attn_fwd.
+ * Errors: INVALID, UNSUPPORTED, CUDA.
+ */
+int attn_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                   const int* block_table, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                   int d, int page_size, int num_pages, int pages_per_seq, int causal,
+                   int window, float scale, cudaStream_t stream, int o_dtype);
+
+/*
  * attn_bwd_workspace_size -- bytes of workspace attn_bwd needs: the f32 row
  * terms D = rowsum(dO * O) [B, Hq, N], 256-byte aligned.  0 on invalid input.
  */

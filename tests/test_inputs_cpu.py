@@ -76,3 +76,18 @@ def test_headline_work_counts():
     per_head = 8192 * 257 - 2 * (128 * 129 // 2)
     assert visible_pairs(8192, False, 128) == per_head
     assert decode_kv_bytes([1 << 20], 8, 128) == 4294967296
+
+
+def test_alternating_layer_groups():
+    """Layer l is global when l % 3 == 0; each group is one global layer and the
+    local layers up to the next global one (two calls per group)."""
+    from exact_transformer_attention_flashattention_b300.alternating import layer_groups
+    assert layer_groups(6) == [(0, 1, 3), (3, 4, 6)]
+    assert layer_groups(5) == [(0, 1, 3), (3, 4, 5)]
+    assert layer_groups(1) == [(0, 1, 1)]
+    assert layer_groups(4, global_every=1) == [(0, 1, 1), (1, 2, 2), (2, 3, 3), (3, 4, 4)]
+    for L in range(1, 12):
+        glob = [g for g, _, _ in layer_groups(L)]
+        assert glob == [l for l in range(L) if l % 3 == 0]
+        covered = sorted(glob + [l for _, a, e in layer_groups(L) for l in range(a, e)])
+        assert covered == list(range(L))
