@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="skip the decode/window sub-objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["backward", "fp8"], default=None,
+    ap.add_argument("--only", choices=["backward", "fp8", "decode", "prefill"], default=None,
                     help="time one extra leg of a prefill workload alone and print its object "
                          "(a small command for kernel profiles; not the benchmark line)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -61,6 +61,14 @@ def parse_args():
     ap.add_argument("--extra-cpu-budget", type=float, default=4.0,
                     help="seconds of oracle work for each sub-workload's cpu_baseline")
     return ap.parse_args()
+
+
+def profile_workloads():
+    """Scaled shapes for ncu captures (a few GB on the device at most): the
+    million-token decode with a quarter of its keys and splits."""
+    from exact_transformer_attention_flashattention_b300.inputs import Workload
+    return {"decode_256k": Workload("decode_256k", "decode", B=1, Hq=32, Hkv=8, N=1 << 18,
+                                    d=128, seed=4, num_splits=512)}
 
 
 def load_peaks():
@@ -714,7 +722,9 @@ def bench_decode(w, steps, warmup, dist, peaks, peak_kind, clocks=None, cpu_budg
     res = {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": ms_full,
            "kv_bytes": kv_bytes, "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
            "frac_of_nameplate_8tbs": round(gbs / NAMEPLATE_HBM_GBS, 4),
-           "kernels": {"decode_partial_kernel_ms": ms_part, "lse_combine_kernel_ms": ms_comb},
+           "kernels": {"decode_partial_kernel_ms": ms_part,
+                       "merge_ms_in_call": round(ms_full - ms_part, 5),
+                       "lse_tree_combine_alone_ms": ms_comb},
            "launches_per_call": 2, "roofline": rf, "timing": timing,
            "config": decode_config(w)}
     if base is not None:
@@ -971,7 +981,8 @@ def decode_config(w):
 def main():
     args = parse_args()
     from exact_transformer_attention_flashattention_b300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload] if args.workload in WORKLOADS else \
+        profile_workloads()[args.workload]
     dist = Dist(args.gpus)
     if args.impl == "reference":
         run_reference(args, w, dist)
@@ -983,8 +994,13 @@ def main():
     from exact_transformer_attention_flashattention_b300 import binding  # noqa: F401 (loads .so)
     peaks, peak_kind = load_peaks()
     if args.only:
-        leg = bench_backward if args.only == "backward" else bench_fp8
-        res = leg(w, args.steps, args.warmup, dist, peaks, peak_kind)
+        if args.only == "decode":
+            res = bench_decode(w, args.steps, args.warmup, dist, peaks, peak_kind)
+        elif args.only == "prefill":
+            res = prefill_extra(w, args.steps, args.warmup, dist, peaks, peak_kind)
+        else:
+            leg = bench_backward if args.only == "backward" else bench_fp8
+            res = leg(w, args.steps, args.warmup, dist, peaks, peak_kind)
         if dist.rank == 0:
             print(json.dumps(res), flush=True)
         dist.close()

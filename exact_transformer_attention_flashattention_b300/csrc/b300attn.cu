@@ -256,23 +256,94 @@ int launch_decode_gt(int GT, const void* kc, const void* vc, const DecodeParams&
   }
 }
 
-int launch_combine(const float* pm, const float* pl, const float* po, void* o, float* lse,
-                   int rows, int S, int d, int o_f32, cudaStream_t stream) {
-  const dim3 grid(rows, d / 32);
-  if (S > 64) {
-    if (d == 128)
-      lse_combine_kernel<128, 32><<<grid, 1024, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
-    else
-      lse_combine_kernel<64, 32><<<grid, 1024, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
-  } else {
-    if (d == 128)
-      lse_combine_kernel<128, 4><<<grid, 128, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
-    else
-      lse_combine_kernel<64, 4><<<grid, 128, 0, stream>>>(pm, pl, po, o, lse, S, o_f32);
+// Many partials: one thread-block cluster of C CTAs per row, C = ceil(S / 256)
+// capped at 8 (a CTA merges at most 256 partials, 16 per warp of 16 warps).
+// Few partials (S <= 64): one warp per row.  With `dependent` the launch is
+// programmatic: it may start while the preceding decode grid still runs, and
+// waits in the kernel for that grid's partials.
+template <int D>
+int launch_combine_t(const float* pm, const float* pl, const float* po, void* o, float* lse,
+                     int rows, int S, int o_f32, bool dependent, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  if (dependent) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (S <= 64) {
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, lse_combine_rows_kernel<D>, pm, pl, po, o, lse, rows, S, o_f32);
+  } else {
+    const int C = std::min(kCombMaxCluster, std::max(1, (S + 255) / 256));
+    if (static_cast<long long>(rows) * C > 0x7fffffffLL)
+      return fail(B300ATTN_ERR_UNSUPPORTED, "too many rows for one combine launch");
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * C), 1, 1);
+    cfg.blockDim = dim3(16 * 32, 1, 1);
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, lse_combine_kernel<D, 16>, pm, pl, po, o, lse, S, o_f32);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return B300ATTN_OK;
+}
+
+int launch_combine(const float* pm, const float* pl, const float* po, void* o, float* lse,
+                   int rows, int S, int d, int o_f32, cudaStream_t stream,
+                   bool dependent = false) {
+  return d == 128 ? launch_combine_t<128>(pm, pl, po, o, lse, rows, S, o_f32, dependent, stream)
+                  : launch_combine_t<64>(pm, pl, po, o, lse, rows, S, o_f32, dependent, stream);
+}
+
+// Number of 64-partial segments of the decode's two-level merge (0: one level).
+int combine_segments(int S) { return S > 64 ? (S + kCombSeg - 1) / kCombSeg : 0; }
+
+// The decode's merge: with more than 64 partials per row, segments of 64 are
+// merged first into the workspace's second-level arrays (many small CTAs, all
+// resident at once), then the segment triples by one warp per row.  Both
+// launches are programmatic (they overlap the end of the grid before them).
+template <int D>
+int launch_decode_combine_t(const DecodeParams& p, void* o, float* lse, int o_f32,
+                            cudaStream_t stream) {
+  const int rows = p.B * p.Hq;
+  const int nseg = combine_segments(p.S);
+  if (nseg == 0)
+    return launch_combine_t<D>(p.part_m, p.part_l, p.part_o, o, lse, rows, p.S, o_f32, true,
+                               stream);
+  if (rows > 65535) return fail(B300ATTN_ERR_UNSUPPORTED, "B*Hq=%d rows > 65535", rows);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(nseg), static_cast<unsigned>(rows), 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_segments_kernel<D>, p.part_m,
+                                           p.part_l, p.part_o, p.seg_m, p.seg_l, p.seg_o, p.S,
+                                           nseg);
+  if (e != cudaSuccess) return cuda_fail(e, "combine (segments) launch");
+  return launch_combine_t<D>(p.seg_m, p.seg_l, p.seg_o, o, lse, rows, nseg, o_f32, true, stream);
+}
+
+int launch_decode_combine(const DecodeParams& p, int d, void* o, float* lse, int o_f32,
+                          cudaStream_t stream) {
+  return d == 128 ? launch_decode_combine_t<128>(p, o, lse, o_f32, stream)
+                  : launch_decode_combine_t<64>(p, o, lse, o_f32, stream);
 }
 
 template <int D>
@@ -355,9 +426,16 @@ int decode_setup(const void* q, const void* k_cache, const void* v_cache, const 
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv_len = kv_len;
-  p.part_m = static_cast<float*>(workspace);
-  p.part_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * 4));
-  p.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * align256(rows * 4));
+  char* ws = static_cast<char*>(workspace);
+  p.part_m = reinterpret_cast<float*>(ws);
+  p.part_l = reinterpret_cast<float*>(ws + align256(rows * 4));
+  p.part_o = reinterpret_cast<float*>(ws + 2 * align256(rows * 4));
+  // second-level triples of the two-level merge, after the partials
+  const size_t srows = static_cast<size_t>(B) * Hq * combine_segments(num_splits);
+  char* lvl2 = ws + 2 * align256(rows * 4) + align256(rows * d * 4);
+  p.seg_m = reinterpret_cast<float*>(lvl2);
+  p.seg_l = reinterpret_cast<float*>(lvl2 + align256(srows * 4));
+  p.seg_o = reinterpret_cast<float*>(lvl2 + 2 * align256(srows * 4));
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -772,7 +850,9 @@ int attn_decode_chunk(int max_kv_len, int num_splits) {
 size_t attn_decode_workspace_size(int B, int Hq, int num_splits, int d) {
   if (B < 0 || Hq < 0 || num_splits < 1 || d < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
-  return 2 * align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+  const size_t srows = static_cast<size_t>(B) * Hq * combine_segments(num_splits);
+  return 2 * align256(rows * sizeof(float)) + align256(rows * d * sizeof(float)) +
+         (srows ? 2 * align256(srows * sizeof(float)) + align256(srows * d * sizeof(float)) : 0);
 }
 
 
@@ -802,8 +882,7 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   if (!aligned16(o) || !aligned16(lse))
     return fail(B300ATTN_ERR_INVALID, "tensor pointers must be 16-byte aligned");
   if ((rc = launch_partials(d, GT, k_cache, v_cache, p, stream)) != B300ATTN_OK) return rc;
-  return launch_combine(p.part_m, p.part_l, p.part_o, o, lse, B * Hq, num_splits, d,
-                        o_dtype == B300ATTN_F32, stream);
+  return launch_decode_combine(p, d, o, lse, o_dtype == B300ATTN_F32, stream);
 }
 
 int attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -863,8 +942,7 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
   p.pages_per_seq = pages_per_seq;
   p.num_pages = num_pages;
   if ((rc = launch_partials(d, GT, k_pages, v_pages, p, stream)) != B300ATTN_OK) return rc;
-  return launch_combine(p.part_m, p.part_l, p.part_o, o, lse, B * Hq, num_splits, d,
-                        o_dtype == B300ATTN_F32, stream);
+  return launch_decode_combine(p, d, o, lse, o_dtype == B300ATTN_F32, stream);
 }
 
 int lse_tree_combine(const float* part_m, const float* part_l, const float* part_o, void* o,
@@ -877,6 +955,11 @@ int lse_tree_combine(const float* part_m, const float* part_l, const float* part
   if (num_splits < 1) return fail(B300ATTN_ERR_INVALID, "num_splits must be >= 1");
   if (!part_m || !part_l || !part_o || !o || !lse)
     return fail(B300ATTN_ERR_INVALID, "NULL tensor pointer");
+  if (!aligned16(part_o) || !aligned16(o))
+    return fail(B300ATTN_ERR_INVALID, "part_o and o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(part_m) & 3u) || (reinterpret_cast<uintptr_t>(part_l) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(B300ATTN_ERR_INVALID, "part_m, part_l and lse must be 4-byte aligned");
   return launch_combine(part_m, part_l, part_o, o, lse, rows, num_splits, d,
                         o_dtype == B300ATTN_F32, stream);
 }

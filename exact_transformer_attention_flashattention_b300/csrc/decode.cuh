@@ -40,6 +40,9 @@ struct DecodeParams {
   float* part_m;           // [B*Hq, S]   natural-log units
   float* part_l;           // [B*Hq, S]
   float* part_o;           // [B*Hq, S, D]
+  float* seg_m;            // [B*Hq, nseg]  second level of the merge (S > 64)
+  float* seg_l;            // [B*Hq, nseg]
+  float* seg_o;            // [B*Hq, nseg, D]
   int B, Hq, Hkv, Lmax, chunk, S, G;
   float scale_log2;
   // Paged cache (block_table != NULL): K/V are [num_pages, page_size, Hkv, D]
@@ -128,6 +131,10 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
   const int hq0 = hkv * p.G + (blockIdx.y % ngroups) * GT;
   const int b = blockIdx.z;
 
+  // The tree combine that follows may launch now: it waits for this whole
+  // grid's partials before reading them (griddepcontrol.wait), so its launch
+  // overlaps this grid's last CTAs instead of following them.
+  grid_launch_dependents();
   int len = p.kv_len[b];
   len = min(max(len, 0), p.Lmax);
   const int key0 = split * p.chunk;
@@ -393,77 +400,264 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
 }
 
 // ---------------------------------------------------------------------------
-// Tree combine: one CTA per (row, 32 columns of d) with NW warps (4 when there
-// are few splits, 32 when there are many).  Each warp folds a strided subset of
-// the partials (eight at a time, merged pairwise), then the NW warp results are
-// merged pairwise in log2(NW) levels through shared memory.
+// Tree combine.  One row's num_splits partials are cut into C contiguous
+// segments (C = 1..8 CTAs, one thread-block cluster per row).  Inside a CTA,
+// a lane owns four consecutive columns of d (one 16-byte load of o per
+// partial; at d = 64 two partials share a warp load), and each warp takes its
+// partials eight at a time: the eight loads of m, l and o are issued together
+// (none depends on another), merged pairwise in three levels, and folded into
+// the warp's running triple.  The NW warp triples are then merged pairwise in
+// log2(NW) levels, and finally CTA 0 of the cluster merges the C CTA triples,
+// read from the other CTAs' shared memory, pairwise in log2(C) levels.
 // ---------------------------------------------------------------------------
 
-struct Triple {
-  float m, l, o;  // m in base-2 units
+constexpr int kCombBatch = 8;
+constexpr int kCombMaxCluster = 8;
+
+struct Triple4 {
+  float m, l;  // m in base-2 units
+  float4 o;
 };
 
-__device__ __forceinline__ Triple lse_merge(Triple a, Triple c) {
+__device__ __forceinline__ Triple4 lse_merge4(Triple4 a, Triple4 c) {
   if (c.m == -INFINITY) return a;
   if (a.m == -INFINITY) return c;
   const float M = fmaxf(a.m, c.m);
   const float wa = ex2_approx(a.m - M), wc = ex2_approx(c.m - M);
-  return Triple{M, fmaf(a.l, wa, c.l * wc), fmaf(a.o, wa, c.o * wc)};
+  Triple4 r;
+  r.m = M;
+  r.l = fmaf(a.l, wa, c.l * wc);
+  r.o = make_float4(fmaf(a.o.x, wa, c.o.x * wc), fmaf(a.o.y, wa, c.o.y * wc),
+                    fmaf(a.o.z, wa, c.o.z * wc), fmaf(a.o.w, wa, c.o.w * wc));
+  return r;
 }
 
+// Few partials per row: one warp per row (four rows per CTA), a lane owns
+// four columns of d, and the row's partials are loaded eight at a time with
+// no branch around the loads; no shared memory and no barrier.
+template <int D>
+__global__ void __launch_bounds__(128)
+    lse_combine_rows_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                            const float* __restrict__ po, void* out, float* lse, int rows, int S,
+                            int o_f32) {
+  constexpr int LPS = D / 4;
+  constexpr int SPW = 32 / LPS;
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int sub = lane / LPS, c4 = lane % LPS;
+  const float* mrow = pm + row * S;
+  const float* lrow = pl + row * S;
+  const float4* orow = reinterpret_cast<const float4*>(po + row * S * D) + c4;
+  Triple4 acc{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int j0 = sub; j0 < S; j0 += SPW * kCombBatch) {
+    Triple4 t[kCombBatch];
+#pragma unroll
+    for (int u = 0; u < kCombBatch; ++u) {
+      const int s = min(j0 + u * SPW, S - 1);
+      t[u].m = __ldg(mrow + s);
+      t[u].l = __ldg(lrow + s);
+      t[u].o = __ldg(orow + static_cast<size_t>(s) * (D / 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kCombBatch; ++u)
+      t[u].m = (j0 + u * SPW < S) ? t[u].m * kLog2e : -INFINITY;
+#pragma unroll
+    for (int w = 1; w < kCombBatch; w <<= 1)
+#pragma unroll
+      for (int u = 0; u + w < kCombBatch; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
+    acc = lse_merge4(acc, t[0]);
+  }
+  if constexpr (SPW == 2) {
+    Triple4 other;
+    other.m = __shfl_xor_sync(0xffffffffu, acc.m, LPS);
+    other.l = __shfl_xor_sync(0xffffffffu, acc.l, LPS);
+    other.o.x = __shfl_xor_sync(0xffffffffu, acc.o.x, LPS);
+    other.o.y = __shfl_xor_sync(0xffffffffu, acc.o.y, LPS);
+    other.o.z = __shfl_xor_sync(0xffffffffu, acc.o.z, LPS);
+    other.o.w = __shfl_xor_sync(0xffffffffu, acc.o.w, LPS);
+    acc = sub ? lse_merge4(other, acc) : lse_merge4(acc, other);
+  }
+  if (sub != 0) return;
+  const float inv = (acc.l > 0.f) ? 1.f / acc.l : 0.f;
+  const float4 v = make_float4(acc.o.x * inv, acc.o.y * inv, acc.o.z * inv, acc.o.w * inv);
+  const size_t oi = static_cast<size_t>(row) * D + 4 * c4;
+  if (o_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = v;
+  } else {
+    uint2 w;
+    w.x = pack_bf16x2(v.x, v.y);
+    w.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + oi) = w;
+  }
+  if (c4 == 0) lse[row] = (acc.l > 0.f) ? (acc.m + __log2f(acc.l)) * kLn2 : -INFINITY;
+}
+
+// First level of the two-level merge used by the decode (which has workspace
+// for it): CTA (segment, row) merges partials [64 seg, 64 seg + 64) of its
+// row -- four warps, sixteen partials each at d = 128, loaded eight at a time
+// -- and writes the segment's triple (m in natural-log units, like a partial)
+// to the second-level arrays, which lse_combine_rows_kernel then merges.
+constexpr int kCombSeg = 64;
+
+template <int D>
+__global__ void __launch_bounds__(128)
+    lse_combine_segments_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                                const float* __restrict__ po, float* m2, float* l2, float* o2,
+                                int S, int nseg) {
+  constexpr int LPS = D / 4;
+  constexpr int SPW = 32 / LPS;
+  constexpr int NW = 4;
+  __shared__ Triple4 red[NW][LPS];
+  grid_dependency_wait();
+  const int seg = blockIdx.x;
+  const long long row = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPS, c4 = lane % LPS;
+  const int sb = seg * kCombSeg, se = min(S, sb + kCombSeg);
+  const float* mrow = pm + row * S;
+  const float* lrow = pl + row * S;
+  const float4* orow = reinterpret_cast<const float4*>(po + row * S * D) + c4;
+  Triple4 acc{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  constexpr int STRIDE = NW * SPW;
+  for (int j0 = sb + warp * SPW + sub; j0 < se; j0 += STRIDE * kCombBatch) {
+    Triple4 t[kCombBatch];
+#pragma unroll
+    for (int u = 0; u < kCombBatch; ++u) {
+      const int s = min(j0 + u * STRIDE, se - 1);
+      t[u].m = __ldg(mrow + s);
+      t[u].l = __ldg(lrow + s);
+      t[u].o = __ldg(orow + static_cast<size_t>(s) * (D / 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kCombBatch; ++u)
+      t[u].m = (j0 + u * STRIDE < se) ? t[u].m * kLog2e : -INFINITY;
+#pragma unroll
+    for (int w = 1; w < kCombBatch; w <<= 1)
+#pragma unroll
+      for (int u = 0; u + w < kCombBatch; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
+    acc = lse_merge4(acc, t[0]);
+  }
+  if constexpr (SPW == 2) {
+    Triple4 other;
+    other.m = __shfl_xor_sync(0xffffffffu, acc.m, LPS);
+    other.l = __shfl_xor_sync(0xffffffffu, acc.l, LPS);
+    other.o.x = __shfl_xor_sync(0xffffffffu, acc.o.x, LPS);
+    other.o.y = __shfl_xor_sync(0xffffffffu, acc.o.y, LPS);
+    other.o.z = __shfl_xor_sync(0xffffffffu, acc.o.z, LPS);
+    other.o.w = __shfl_xor_sync(0xffffffffu, acc.o.w, LPS);
+    acc = sub ? lse_merge4(other, acc) : lse_merge4(acc, other);
+  }
+  if (sub == 0) red[warp][c4] = acc;
+  __syncthreads();
+  if (threadIdx.x < LPS) {  // the four warp triples, pairwise in two levels
+    const Triple4 a = lse_merge4(red[0][threadIdx.x], red[1][threadIdx.x]);
+    const Triple4 b = lse_merge4(red[2][threadIdx.x], red[3][threadIdx.x]);
+    const Triple4 r = lse_merge4(a, b);
+    const size_t si = static_cast<size_t>(row) * nseg + seg;
+    reinterpret_cast<float4*>(o2 + si * D)[threadIdx.x] = r.o;
+    if (threadIdx.x == 0) {
+      m2[si] = (r.m == -INFINITY) ? -INFINITY : r.m * kLn2;
+      l2[si] = r.l;
+    }
+  }
+}
+
+// grid.x = rows * C with clusters of C CTAs along x: CTA (row, segment).
 template <int D, int NW>
 __global__ void __launch_bounds__(NW * 32)
     lse_combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                        const float* __restrict__ po, void* out, float* lse, int S, int o_f32) {
-  __shared__ Triple red[NW][32];
-  const int row = blockIdx.x;
+  constexpr int LPS = D / 4;     // lanes per partial (four columns each)
+  constexpr int SPW = 32 / LPS;  // partials per warp load
+  __shared__ Triple4 red[NW][LPS];
+  __shared__ Triple4 cta_res[LPS];
+  grid_dependency_wait();  // the partials of a preceding decode grid are complete
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t csize = cluster_nctarank();
+  const long long row = blockIdx.x / csize;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = blockIdx.y * 32 + lane;
-  const float* mrow = pm + static_cast<size_t>(row) * S;
-  const float* lrow = pl + static_cast<size_t>(row) * S;
-  const float* orow = po + static_cast<size_t>(row) * S * D + col;
+  const int sub = lane / LPS, c4 = lane % LPS;
+  const int per = (S + static_cast<int>(csize) - 1) / static_cast<int>(csize);
+  const int sb = static_cast<int>(rank) * per, se = min(S, sb + per);
+  const float* mrow = pm + row * S;
+  const float* lrow = pl + row * S;
+  const float4* orow = reinterpret_cast<const float4*>(po + row * S * D) + c4;
 
-  Triple acc{-INFINITY, 0.f, 0.f};
-  constexpr int BATCH = 8;
-  for (int s0 = warp; s0 < S; s0 += NW * BATCH) {
-    Triple t[BATCH];
+  Triple4 acc{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  constexpr int STRIDE = NW * SPW;
+  for (int j0 = sb + warp * SPW + sub; j0 < se; j0 += STRIDE * kCombBatch) {
+    Triple4 t[kCombBatch];
+    // All 3 x 8 loads are issued before any is used: no branch around them
+    // (an index past the segment is clamped, and its triple masked to the
+    // identity afterwards), so they are all in flight together.
 #pragma unroll
-    for (int u = 0; u < BATCH; ++u) {
-      const int s = s0 + u * NW;
-      t[u] = Triple{-INFINITY, 0.f, 0.f};
-      if (s < S) {
-        const float m = mrow[s];
-        t[u].m = (m == -INFINITY) ? -INFINITY : m * kLog2e;
-        if (t[u].m != -INFINITY) {
-          t[u].l = lrow[s];
-          t[u].o = orow[static_cast<size_t>(s) * D];
-        }
+    for (int u = 0; u < kCombBatch; ++u) {
+      const int s = min(j0 + u * STRIDE, se - 1);
+      t[u].m = __ldg(mrow + s);
+      t[u].l = __ldg(lrow + s);
+      t[u].o = __ldg(orow + static_cast<size_t>(s) * (D / 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kCombBatch; ++u)  // -inf stays -inf: an empty split, its o never used
+      t[u].m = (j0 + u * STRIDE < se) ? t[u].m * kLog2e : -INFINITY;
+#pragma unroll
+    for (int w = 1; w < kCombBatch; w <<= 1)
+#pragma unroll
+      for (int u = 0; u + w < kCombBatch; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
+    acc = lse_merge4(acc, t[0]);
+  }
+  if constexpr (SPW == 2) {  // the two partials of a warp load share columns
+    Triple4 other;
+    other.m = __shfl_xor_sync(0xffffffffu, acc.m, LPS);
+    other.l = __shfl_xor_sync(0xffffffffu, acc.l, LPS);
+    other.o.x = __shfl_xor_sync(0xffffffffu, acc.o.x, LPS);
+    other.o.y = __shfl_xor_sync(0xffffffffu, acc.o.y, LPS);
+    other.o.z = __shfl_xor_sync(0xffffffffu, acc.o.z, LPS);
+    other.o.w = __shfl_xor_sync(0xffffffffu, acc.o.w, LPS);
+    acc = sub ? lse_merge4(other, acc) : lse_merge4(acc, other);
+  }
+  if (sub == 0) red[warp][c4] = acc;
+  __syncthreads();
+#pragma unroll
+  for (int w = NW / 2; w >= 1; w >>= 1) {  // warp triples, pairwise in log2(NW) levels
+    if (warp < w && sub == 0) red[warp][c4] = lse_merge4(red[warp][c4], red[warp + w][c4]);
+    __syncthreads();
+  }
+  if (threadIdx.x < LPS) cta_res[threadIdx.x] = red[0][threadIdx.x];
+  cluster_sync_all();  // every CTA's triple is in its shared memory
+  if (rank == 0 && threadIdx.x < LPS) {
+    Triple4 t[kCombMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kCombMaxCluster; ++r) {
+      t[r].m = -INFINITY;
+      if (r < static_cast<int>(csize)) {
+        const uint32_t a = dsmem_map(&cta_res[threadIdx.x], static_cast<uint32_t>(r));
+        t[r].m = ld_dsmem_f32(a + offsetof(Triple4, m));
+        t[r].l = ld_dsmem_f32(a + offsetof(Triple4, l));
+        t[r].o = ld_dsmem_f32x4(a + offsetof(Triple4, o));
       }
     }
 #pragma unroll
-    for (int w = 1; w < BATCH; w <<= 1)
+    for (int w = 1; w < kCombMaxCluster; w <<= 1)
 #pragma unroll
-      for (int u = 0; u + w < BATCH; u += 2 * w) t[u] = lse_merge(t[u], t[u + w]);
-    acc = lse_merge(acc, t[0]);
+      for (int u = 0; u + w < kCombMaxCluster; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
+    const Triple4 r = t[0];
+    const float inv = (r.l > 0.f) ? 1.f / r.l : 0.f;
+    const float4 v = make_float4(r.o.x * inv, r.o.y * inv, r.o.z * inv, r.o.w * inv);
+    const size_t oi = static_cast<size_t>(row) * D + 4 * threadIdx.x;
+    if (o_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = v;
+    } else {
+      uint2 w;
+      w.x = pack_bf16x2(v.x, v.y);
+      w.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + oi) = w;
+    }
+    if (threadIdx.x == 0) lse[row] = (r.l > 0.f) ? (r.m + __log2f(r.l)) * kLn2 : -INFINITY;
   }
-  red[warp][lane] = acc;
-  __syncthreads();
-#pragma unroll
-  for (int w = NW / 2; w >= 1; w >>= 1) {
-    if (warp < w) red[warp][lane] = lse_merge(red[warp][lane], red[warp + w][lane]);
-    __syncthreads();
-  }
-  if (warp == 0) {
-    const Triple r = red[0][lane];
-    const float val = (r.l > 0.f) ? r.o / r.l : 0.f;
-    const size_t oi = static_cast<size_t>(row) * D + col;
-    if (o_f32)
-      static_cast<float*>(out)[oi] = val;
-    else
-      static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(val);
-    if (blockIdx.y == 0 && lane == 0)
-      lse[row] = (r.l > 0.f) ? (r.m + __log2f(r.l)) * kLn2 : -INFINITY;
-  }
+  cluster_sync_all();  // CTA 0 has read the others' shared memory before they exit
 }
 
 }  // namespace b300

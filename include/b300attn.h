@@ -236,7 +236,10 @@ int attn_decode_chunk(int max_kv_len, int num_splits);
 /*
  * attn_decode_workspace_size -- bytes of workspace attn_decode_splitkv needs
  * for the split partials: f32 m and l [B, Hq, num_splits] and f32 o
- * [B, Hq, num_splits, d], each region 256-byte aligned.  0 on invalid input.
+ * [B, Hq, num_splits, d], each region 256-byte aligned; with more than 64
+ * splits, followed by the second level of the merge (the same three arrays
+ * with nseg = ceil(num_splits / 64) in place of num_splits).  0 on invalid
+ * input.
  */
 size_t attn_decode_workspace_size(int B, int Hq, int num_splits, int d);
 
@@ -248,9 +251,10 @@ size_t attn_decode_workspace_size(int B, int Hq, int num_splits, int d);
  * (sequence, kv head, chunk), the partial triple of every query head in the
  * group -- m = max score, l = sum exp(s - m), o = sum exp(s - m) v -- streaming
  * each K/V byte once per group; a second kernel merges the partials with the
- * logsumexp tree of lse_tree_combine.  The split and the tree follow the Tree
- * Attention page (express24.ir), abstract: the reduction along the sequence
- * axis is associative and can be computed as a tree.
+ * logsumexp tree (two levels when there are more than 64 splits: segments of
+ * 64 partials, then the segment triples).  The split and the tree follow the
+ * Tree Attention page (express24.ir), abstract: the reduction along the
+ * sequence axis is associative and can be computed as a tree.
  *
  *   q        bf16 [B, Hq, d]
  *   k_cache, v_cache  bf16 [B, max_kv_len, Hkv, d]; only rows < kv_len[b] are read
@@ -283,8 +287,8 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
  * loads the library holds that array until the process exits.  A call whose
  * partials would need more than that (attn_decode_workspace_size(B, Hq,
  * num_splits, d) > 40 MiB) returns B300ATTN_ERR_WORKSPACE with a message; e.g.
- * 1 sequence x 32 heads x 2048 splits x d=128 needs 32.5 MiB
- * (34,078,720 bytes) and fits.
+ * 1 sequence x 32 heads x 2048 splits x d=128 needs 33.0 MiB
+ * (34,611,200 bytes) and fits.
  *
  * The first call on a device looks up the scratch array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
@@ -355,9 +359,13 @@ int attn_decode_partials(const void* q, const void* k_cache, const void* v_cache
  * writes O = o / l and LSE = M + ln l.  A partial with m = -inf is the empty
  * identity and its o is never read.
  *
+ * One thread-block cluster of up to 8 CTAs merges a row: each CTA a
+ * contiguous segment of the partials, the CTAs' triples merged through
+ * distributed shared memory.
+ *
  *   part_m, part_l  f32 [rows, num_splits]   (m in natural-log units)
- *   part_o          f32 [rows, num_splits, d]
- *   o               [rows, d] bf16 or f32 (o_dtype);  lse  f32 [rows]
+ *   part_o          f32 [rows, num_splits, d], 16-byte aligned
+ *   o               [rows, d] bf16 or f32 (o_dtype), 16-byte aligned;  lse  f32 [rows]
  *   d in {64, 128}; num_splits >= 1.
  * Errors: INVALID, UNSUPPORTED, CUDA.
  */

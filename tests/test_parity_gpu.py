@@ -146,6 +146,8 @@ DECODE_CASES = [
     (2, 12, 2, 400, 128, 3, [400, 150], True),        # six heads per group: 3 CTAs of 2
     (1, 4, 1, 4096, 128, 1, [4096], True),            # a single split
     (1, 8, 2, 2048, 64, 64, [2000], False),           # many small splits
+    (2, 8, 2, 6400, 128, 100, [6400, 777], True),     # > 64 splits: two-level merge
+    (1, 4, 2, 9000, 64, 300, [8999], False),          # two levels, five segments, d=64
 ]
 
 
