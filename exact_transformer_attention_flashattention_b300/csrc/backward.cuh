@@ -94,6 +94,19 @@ __device__ __forceinline__ bool bwd_visible(int q, int k, int N, bool causal, in
   return true;
 }
 
+// CTA x of a grid of nt tiles x BH heads: heads in groups of kBwdHeadGroup,
+// tile-major inside a group (tile index t, head index bh).
+constexpr int kBwdHeadGroup = 8;
+__device__ __forceinline__ void bwd_order(unsigned x, int nt, int BH, int& t, int& bh) {
+  const int per = kBwdHeadGroup * nt;
+  const int g = static_cast<int>(x / per);
+  const int gbase = g * kBwdHeadGroup;
+  const int gsz = min(kBwdHeadGroup, BH - gbase);
+  const int r = static_cast<int>(x - static_cast<unsigned>(g) * per);
+  t = r / gsz;
+  bh = gbase + r % gsz;
+}
+
 template <int D>
 struct BwdCfg {
   static constexpr int TILE = 128;                  // rows of a Q, dO, K or V tile
@@ -142,11 +155,12 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int nkt = (N + 127) / 128;
-  // Causal: the first key tiles are seen by the most query tiles, so the
-  // launch order is tile-major from the first key tile (heaviest CTAs first).
-  const int BH = p.B * p.Hkv;
-  const int jt = p.causal ? static_cast<int>(blockIdx.x / BH) : static_cast<int>(blockIdx.x % nkt);
-  const int bh = p.causal ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / nkt);
+  // Launch order: (sequence, kv head) pairs in groups of kBwdHeadGroup; within
+  // a group, key tile by key tile from the first (under a causal mask the
+  // first key tiles are seen by the most query tiles: heaviest CTAs first), so
+  // the CTAs resident at one time share a few heads' Q and dO in L2.
+  int jt, bh;
+  bwd_order(blockIdx.x, nkt, p.B * p.Hkv, jt, bh);
   const int hk = bh % p.Hkv;
   const int b = bh / p.Hkv;
   const int G = p.Hq / p.Hkv;
@@ -451,12 +465,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int nqt = (N + 127) / 128;
-  // Causal: the last query tiles see the most key tiles, so the launch order
-  // is tile-major from the last query tile (heaviest CTAs first).
-  const int BH = p.B * p.Hq;
-  const int it = p.causal ? nqt - 1 - static_cast<int>(blockIdx.x / BH)
-                          : static_cast<int>(blockIdx.x % nqt);
-  const int bh = p.causal ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / nqt);
+  // Launch order as for dK/dV (groups of heads, tile by tile within a group),
+  // from the last query tile: under a causal mask it sees the most key tiles.
+  int it, bh;
+  bwd_order(blockIdx.x, nqt, p.B * p.Hq, it, bh);
+  if (p.causal) it = nqt - 1 - it;
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;
   const int hk = h / (p.Hq / p.Hkv);
