@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
 // ---------------------------------------------------------------------------
 
 constexpr int kCombBatch = 8;
+constexpr int kRowsBatch = 16;
 constexpr int kCombMaxCluster = 8;
 
 struct Triple4 {
@@ -433,8 +434,9 @@ __device__ __forceinline__ Triple4 lse_merge4(Triple4 a, Triple4 c) {
 }
 
 // Few partials per row: one warp per row (four rows per CTA), a lane owns
-// four columns of d, and the row's partials are loaded eight at a time with
-// no branch around the loads; no shared memory and no barrier.
+// four columns of d, and the row's partials are loaded sixteen at a time (at
+// d = 128 the whole row of a 16-split decode in one round trip) with no
+// branch around the loads; no shared memory and no barrier.
 template <int D>
 __global__ void __launch_bounds__(128)
     lse_combine_rows_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
@@ -451,22 +453,22 @@ __global__ void __launch_bounds__(128)
   const float* lrow = pl + row * S;
   const float4* orow = reinterpret_cast<const float4*>(po + row * S * D) + c4;
   Triple4 acc{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-  for (int j0 = sub; j0 < S; j0 += SPW * kCombBatch) {
-    Triple4 t[kCombBatch];
+  for (int j0 = sub; j0 < S; j0 += SPW * kRowsBatch) {
+    Triple4 t[kRowsBatch];
 #pragma unroll
-    for (int u = 0; u < kCombBatch; ++u) {
+    for (int u = 0; u < kRowsBatch; ++u) {
       const int s = min(j0 + u * SPW, S - 1);
       t[u].m = __ldg(mrow + s);
       t[u].l = __ldg(lrow + s);
       t[u].o = __ldg(orow + static_cast<size_t>(s) * (D / 4));
     }
 #pragma unroll
-    for (int u = 0; u < kCombBatch; ++u)
+    for (int u = 0; u < kRowsBatch; ++u)
       t[u].m = (j0 + u * SPW < S) ? t[u].m * kLog2e : -INFINITY;
 #pragma unroll
-    for (int w = 1; w < kCombBatch; w <<= 1)
+    for (int w = 1; w < kRowsBatch; w <<= 1)
 #pragma unroll
-      for (int u = 0; u + w < kCombBatch; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
+      for (int u = 0; u + w < kRowsBatch; u += 2 * w) t[u] = lse_merge4(t[u], t[u + w]);
     acc = lse_merge4(acc, t[0]);
   }
   if constexpr (SPW == 2) {
