@@ -84,10 +84,23 @@ def load_peaks():
 # device-code files each profiled kernel is compiled from
 KERNEL_SOURCES = {
     "prefill_kernel": ("prefill.cuh", "ptx.cuh"),
+    "prefill_band_kernel": ("band.cuh", "prefill.cuh", "ptx.cuh"),
     "decode_partial_kernel": ("decode.cuh", "ptx.cuh"),
     "bwd_dkdv_kernel": ("backward.cuh", "ptx.cuh"),
     "fp8_quantize_kernel": ("fp8.cuh", "ptx.cuh"),
 }
+
+
+# Widest window (keys on each side) that attn_fwd sends to the band kernel.
+BAND_MAX_WINDOW = 256
+
+
+def prefill_kernel_name(d: int, causal: bool, window: int) -> str:
+    """The kernel attn_fwd runs for a dense bf16 prefill: the band kernel for a
+    short non-causal window at d = 64, prefill_kernel otherwise."""
+    if d == 64 and not causal and 0 <= window <= BAND_MAX_WINDOW:
+        return "prefill_band_kernel"
+    return "prefill_kernel"
 
 
 def kernel_source_sha(kernel: str = "prefill_kernel"):
@@ -447,8 +460,9 @@ def bench_prefill(w, steps, warmup, dist, peaks, peak_kind, clocks=None):
     assert fa.device_status() == 0, fa.last_error()
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    rf = roofline(tflops, peak, "TFLOP/s", "tensor",
-                  stored_traffic("prefill_kernel", w.name), flops, "FLOP")
+    kname = prefill_kernel_name(w.d, w.causal, w.window)
+    rf = roofline(tflops, peak, "TFLOP/s", "tensor", stored_traffic(kname, w.name), flops, "FLOP")
+    rf["kernel"] = kname
     rf["peak_kind"] = f"{peak_kind} dense bf16 (burst)"
     rf["frac_of_sustained"] = round(tflops / peaks.get("bf16_tflops_sustained", peak), 4)
     io_bytes = (q.numel() + k.numel() + v.numel()) * 2 + o.numel() * o.element_size() + lse.numel() * 4

@@ -15,6 +15,7 @@
 
 #include "b300attn.h"
 #include "backward.cuh"
+#include "band.cuh"
 #include "decode.cuh"
 #include "fp8.cuh"
 #include "prefill.cuh"
@@ -161,6 +162,43 @@ int launch_prefill(const void* q, const void* k, const void* v, const PrefillPar
   kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return B300ATTN_OK;
+}
+
+// Widest window (keys on each side) that the band schedule takes: a Q tile
+// then sees at most five key tiles.
+constexpr int kBandMaxWindow = 256;
+
+// Short non-causal window at d = 64, dense layout: the two-stream band kernel.
+// A bf16 O is written by TMA through a 4-D map [B][N][Hq][64], so that a
+// tile's rows past N are clipped at its own sequence's end.
+int launch_prefill_band(const void* q, const void* k, const void* v, const PrefillParams& p,
+                        cudaStream_t stream) {
+  using C = BandCfg<64>;
+  CUtensorMap tq, tk, tv, to;
+  int rc;
+  if ((rc = make_map_3d(&tq, q, 64, p.Hq, p.total_rows, 64, 1, C::BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_3d(&tk, k, 64, p.Hkv, p.total_rows, 64, 1, C::BN,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k")) != B300ATTN_OK)
+    return rc;
+  if ((rc = make_map_3d(&tv, v, 64, p.Hkv, p.total_rows, 64, 1, C::BN,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
+    return rc;
+  if (p.o_f32)
+    to = tq;  // not read: an f32 O is written with plain stores
+  else if ((rc = make_map_4d(&to, p.o, 64, p.Hq, p.N, p.B, 64, 1, C::BM, 1,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "o")) != B300ATTN_OK)
+    return rc;
+  if ((rc = set_smem(prefill_band_kernel<64>, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != B300ATTN_OK) return rc;
+  const long long tiles = static_cast<long long>(p.B) * p.Hq * ((p.N + 127) / 128);
+  const int grid = static_cast<int>(std::min<long long>((tiles + 1) / 2, sms));
+  prefill_band_kernel<64><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "band prefill launch");
   return B300ATTN_OK;
 }
 
@@ -558,6 +596,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   const long long items = static_cast<long long>(p.nqb) * Hq * B;
   if (items > 0x7fffffffLL) return fail(B300ATTN_ERR_UNSUPPORTED, "too many query blocks");
   p.n_items = static_cast<int>(items);
+  const long long q_tiles = static_cast<long long>(B) * Hq * ((N + 127) / 128);
+  if (d == 64 && !causal && p.window >= 0 && p.window <= kBandMaxWindow &&
+      q_tiles <= 0x7fffffffLL)
+    return launch_prefill_band(q, k, v, p, stream);
   return d == 128 ? launch_prefill<128>(q, k, v, p, p.n_items, stream)
                   : launch_prefill<64>(q, k, v, p, p.n_items, stream);
 }

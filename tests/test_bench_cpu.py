@@ -30,6 +30,23 @@ def test_kernel_source_sha_is_per_kernel():
             assert os.path.exists(os.path.join(bench.ROOT, bench.PKG, "csrc", f)), f
 
 
+def test_prefill_kernel_name_follows_the_library_dispatch():
+    """bench.py names the kernel a prefill workload runs with the same rule as
+    attn_fwd: the band kernel for a non-causal window of at most the library's
+    kBandMaxWindow keys per side at d = 64."""
+    import re
+    src = open(os.path.join(bench.ROOT, bench.PKG, "csrc", "b300attn.cu")).read()
+    m = re.search(r"constexpr int kBandMaxWindow = (\d+);", src)
+    assert m and int(m.group(1)) == bench.BAND_MAX_WINDOW
+    name = bench.prefill_kernel_name
+    assert name(64, False, 128) == "prefill_band_kernel"
+    assert name(64, False, 0) == "prefill_band_kernel"
+    assert name(64, False, bench.BAND_MAX_WINDOW + 1) == "prefill_kernel"
+    assert name(64, False, -1) == "prefill_kernel"
+    assert name(64, True, 128) == "prefill_kernel"
+    assert name(128, False, 128) == "prefill_kernel"
+
+
 def test_stored_traffic_needs_matching_device_code(tmp_path, monkeypatch):
     """A traffic row is returned only when kernel, workload and source hash
     all match; a changed kernel (different hash) yields None."""

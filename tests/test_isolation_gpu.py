@@ -46,6 +46,7 @@ DENSE = [
     (2, 2, 2, 300, 64, False, -1),
     (3, 4, 2, 200, 128, False, 50),
     (2, 2, 1, 129, 64, True, 100),
+    (2, 2, 2, 300, 64, False, 100),   # short non-causal window at d = 64
 ]
 
 

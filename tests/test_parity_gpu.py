@@ -63,6 +63,13 @@ PREFILL_CASES = [
     # large scores (peaked rows, rescaling exercised); f32 O, because bf16
     # rounding of |O| up to ~4 alone costs 2^-9 * 4 = 0.008 of the 0.01 budget
     (1, 4, 4, 1536, 128, False, -1, True, 0.5),
+    # short non-causal windows at d = 64 (the two-stream band schedule)
+    (2, 4, 2, 300, 64, False, 50, True, None),
+    (1, 2, 2, 129, 64, False, 0, False, None),
+    (2, 2, 1, 1000, 64, False, 256, True, None),
+    (1, 3, 3, 1025, 64, False, 128, False, None),
+    (3, 2, 2, 640, 64, False, 128, True, 0.5),
+    (1, 1, 1, 1, 64, False, 64, True, None),
 ]
 
 
@@ -121,18 +128,30 @@ def test_prefill_is_deterministic(fa):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_prefill_writes_only_its_outputs(fa):
-    """Guard regions around O and LSE keep their sentinel values."""
-    B, H, N, d, G = 1, 2, 300, 128, 4096
+@pytest.mark.parametrize("d,causal,window,dtype", [
+    (128, True, -1, torch.bfloat16),
+    (64, False, 128, torch.bfloat16),   # short window at d = 64: O leaves by TMA store
+    (64, False, 128, torch.float32),
+], ids=["d128-causal", "d64-window-bf16", "d64-window-f32"])
+def test_prefill_writes_only_its_outputs(fa, d, causal, window, dtype):
+    """Guard regions around O and LSE keep their sentinel values.  N = 300
+    leaves the last 128-row tile 84 rows short; each guard holds a whole tile,
+    so that a write past the end would land inside the allocation."""
+    B, H, N = 1, 2, 300
+    G, GL = 128 * H * d, 4096
     q, k, v = (t.cuda() for t in prefill_inputs(B, H, H, N, d, seed=9))
-    o_buf = torch.full((G + B * N * H * d + G,), 7.0, dtype=torch.bfloat16, device="cuda")
-    l_buf = torch.full((G + B * H * N + G,), 7.0, dtype=torch.float32, device="cuda")
+    o_buf = torch.full((G + B * N * H * d + G,), 7.0, dtype=dtype, device="cuda")
+    l_buf = torch.full((GL + B * H * N + GL,), 7.0, dtype=torch.float32, device="cuda")
     O = o_buf[G:G + B * N * H * d].view(B, N, H, d)
-    L = l_buf[G:G + B * H * N].view(B, H, N)
-    fa.attn_fwd(q, k, v, causal=True, out=O, lse=L)
+    L = l_buf[GL:GL + B * H * N].view(B, H, N)
+    fa.attn_fwd(q, k, v, causal=causal, window=window, out=O, lse=L)
     torch.cuda.synchronize()
-    for buf in (o_buf, l_buf):
-        assert torch.all(buf[:G] == 7.0) and torch.all(buf[-G:] == 7.0)
+    assert fa.device_status() == 0
+    for buf, g in ((o_buf, G), (l_buf, GL)):
+        assert torch.all(buf[:g] == 7.0) and torch.all(buf[-g:] == 7.0)
+    O_ref, L_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, window=window,
+                                    scale=1.0 / math.sqrt(d))
+    assert_close(O, L, O_ref, L_ref, f"d={d} window={window} {dtype}")
 
 
 # ------------------------------------------------------------------ decode
