@@ -406,14 +406,19 @@ __global__ void __launch_bounds__(384, 1)
         if (kv0 + BN > p.N || t.r0 + 127 - kv0 > window || kv0 + BN - 1 - t.r0 > window) {
           const int lo_c = max(0, row - window) - kv0;
           const int hi_c = min(p.N - 1, row + window) - kv0;
+          // the warp's extreme bounds decide each chunk's class uniformly
+          const int lo_min = __reduce_min_sync(0xffffffffu, lo_c);
+          const int lo_max = __reduce_max_sync(0xffffffffu, lo_c);
+          const int hi_min = __reduce_min_sync(0xffffffffu, hi_c);
+          const int hi_max = __reduce_max_sync(0xffffffffu, hi_c);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int a = lo_c - 32 * q, b = hi_c - 32 * q;  // visible: a <= e <= b
-            if (__all_sync(0xffffffffu, a <= 0 && b >= 31)) continue;
-            if (__all_sync(0xffffffffu, a > 31 || b < 0)) {
+            if (lo_max <= 32 * q && hi_min >= 32 * q + 31) continue;
+            if (lo_min > 32 * q + 31 || hi_max < 32 * q) {
               empty |= 1u << q;
               continue;
             }
+            const int a = lo_c - 32 * q, b = hi_c - 32 * q;  // visible: a <= e <= b
             const uint32_t hi_bits = b >= 31 ? 0xffffffffu : (b < 0 ? 0u : (2u << b) - 1u);
             const uint32_t lo_bits = a <= 0 ? 0xffffffffu : (a > 31 ? 0u : ~((1u << a) - 1u));
             const uint32_t vis = hi_bits & lo_bits;
@@ -422,14 +427,22 @@ __global__ void __launch_bounds__(384, 1)
               x[32 * q + e] = (vis & (1u << e)) ? x[32 * q + e] : -INFINITY;
           }
         }
-        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // row maximum: eight independent chains, then empty chunks dropped (their
+        // scores were not masked)
+        float mc[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (empty & (1u << q)) continue;
+        for (int k = 0; k < 8; ++k)  // chain k: chunk k / 2, column pairs 2 (k % 2) + 4 i
+          mc[k] = fmaxf(x[32 * (k >> 1) + 2 * (k & 1)], x[32 * (k >> 1) + 2 * (k & 1) + 1]);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) mc[q] = fmax3(mc[q], x[32 * q + e], x[32 * q + e + 1]);
-        }
-        const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
+        for (int e = 4; e < 32; e += 4)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mc[k] = fmax3(mc[k], x[32 * (k >> 1) + e + 2 * (k & 1)],
+                          x[32 * (k >> 1) + e + 2 * (k & 1) + 1]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          mc[2 * q] = (empty & (1u << q)) ? -INFINITY : fmaxf(mc[2 * q], mc[2 * q + 1]);
+        const float mx = fmaxf(fmaxf(mc[0], mc[2]), fmaxf(mc[4], mc[6]));
         const float m_new = fmaxf(m_ref, mx * c);
         const bool resc = m_new > m_ref + kRescaleThreshold;
         float alpha = 1.f;
