@@ -84,7 +84,8 @@ def load_peaks():
 # device-code files each profiled kernel is compiled from
 KERNEL_SOURCES = {
     "prefill_kernel": ("prefill.cuh", "ptx.cuh"),
-    "prefill_band_kernel": ("band.cuh", "prefill.cuh", "ptx.cuh"),
+    # (+ the host file that sets its tensor maps' L2 fetch granule)
+    "prefill_band_kernel": ("band.cuh", "prefill.cuh", "ptx.cuh", "b300attn.cu"),
     "decode_partial_kernel": ("decode.cuh", "ptx.cuh"),
     "bwd_dkdv_kernel": ("backward.cuh", "ptx.cuh"),
     "fp8_quantize_kernel": ("fp8.cuh", "ptx.cuh"),

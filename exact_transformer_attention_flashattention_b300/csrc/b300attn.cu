@@ -76,10 +76,13 @@ int make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
 }
 
 // 3-D tensor map over a row-major [d2][d1][d0] array (d0 contiguous) of bf16
-// elements, or of bytes when `bytes` is set (e4m3 codes).
+// elements, or of bytes when `bytes` is set (e4m3 codes).  `promo` is the L2
+// fetch granule: 256 B by default; 128 B for 128-byte rows whose neighbours
+// (the next head's row) are read by another CTA much later.
 int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                 uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swizzle,
-                const char* name, bool bytes = false) {
+                const char* name, bool bytes = false,
+                CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const uint64_t es = bytes ? 1 : 2;
@@ -90,7 +93,7 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   const CUresult r = fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(B300ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
                 static_cast<int>(r));
@@ -143,15 +146,18 @@ int launch_prefill(const void* q, const void* k, const void* v, const PrefillPar
   using C = PrefillCfg<D>;
   CUtensorMap tq, tk, tv;
   int rc;
-  // q, k, v seen as [rows, heads, d]; tiles of 128 rows x 64 elements of d
+  // q, k, v seen as [rows, heads, d]; tiles of 128 rows x 64 elements of d.
+  // At d = 64 a row is 128 B: fetch it alone, not with the next head's row.
+  const CUtensorMapL2promotion promo =
+      D == 64 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   if ((rc = make_map_3d(&tq, q, D, p.Hq, p.total_rows, 64, 1, C::BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q", false, promo)) != B300ATTN_OK)
     return rc;
   if ((rc = make_map_3d(&tk, k, D, p.Hkv, p.total_rows, 64, 1, C::BN,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "k")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k", false, promo)) != B300ATTN_OK)
     return rc;
   if ((rc = make_map_3d(&tv, v, D, p.Hkv, p.total_rows, 64, 1, C::BN,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v", false, promo)) != B300ATTN_OK)
     return rc;
   auto kernel = p.cu_seqlens ? prefill_kernel<D, true> : prefill_kernel<D, false>;
   if ((rc = set_smem(kernel, C::SMEM_BYTES)) != B300ATTN_OK) return rc;
@@ -177,14 +183,16 @@ int launch_prefill_band(const void* q, const void* k, const void* v, const Prefi
   using C = BandCfg<64>;
   CUtensorMap tq, tk, tv, to;
   int rc;
+  // rows are 128 B (d = 64): fetch them alone, not with the next head's row
+  const CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   if ((rc = make_map_3d(&tq, q, 64, p.Hq, p.total_rows, 64, 1, C::BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "q")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "q", false, promo)) != B300ATTN_OK)
     return rc;
   if ((rc = make_map_3d(&tk, k, 64, p.Hkv, p.total_rows, 64, 1, C::BN,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "k")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "k", false, promo)) != B300ATTN_OK)
     return rc;
   if ((rc = make_map_3d(&tv, v, 64, p.Hkv, p.total_rows, 64, 1, C::BN,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "v")) != B300ATTN_OK)
+                        CU_TENSOR_MAP_SWIZZLE_128B, "v", false, promo)) != B300ATTN_OK)
     return rc;
   if (p.o_f32)
     to = tq;  // not read: an f32 O is written with plain stores
