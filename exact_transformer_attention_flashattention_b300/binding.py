@@ -15,7 +15,12 @@ import os
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libb300attn.so")
+_HERE = os.path.dirname(os.path.abspath(__file__))
+RELEASE_LIB_PATH = os.path.join(_HERE, "libb300attn.so")
+# B300ATTN_DEBUG=1 selects the debug build (device-side checks reported by
+# attn_device_status; built by `python -m ...build --debug`)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libb300attn_debug.so")
+LIB_PATH = DEBUG_LIB_PATH if os.environ.get("B300ATTN_DEBUG") == "1" else RELEASE_LIB_PATH
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 BF16, F32 = 0, 1

@@ -1,6 +1,12 @@
 """Compile the CUDA library in-tree: libb300attn.so next to this file, sm_103a only.
 
-    python -m exact_transformer_attention_flashattention_b300.build [--force]
+    python -m exact_transformer_attention_flashattention_b300.build [--force] [--debug]
+
+`--debug` builds libb300attn_debug.so instead: the same library compiled with
+-DB300ATTN_DEBUG, whose kernels also check caller data they otherwise clamp
+(kv_len, cu_seqlens) and their own index invariants, and report a failed check
+through attn_device_status (see csrc/debug.cuh).  The binding loads it when
+the environment variable B300ATTN_DEBUG is 1.
 """
 
 from __future__ import annotations
@@ -15,6 +21,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libb300attn.so")
+LIB_DEBUG = os.path.join(HERE, "libb300attn_debug.so")
 SOURCE = os.path.join(CSRC, "b300attn.cu")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,19 +42,27 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the shared library if any source is newer; return its path."""
-    if not force and up_to_date():
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *FLAGS, *ARCH, "-o", tmp, SOURCE]
+def nvcc_command(out: str, debug: bool = False) -> list:
+    """The nvcc command line that builds the library (or its debug variant) into `out`."""
+    return [_nvcc(), *FLAGS, *(["-DB300ATTN_DEBUG"] if debug else []), *ARCH, "-o", out, SOURCE]
+
+
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Build the shared library (or its debug variant) if any source is newer;
+    return its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(debug):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = nvcc_command(tmp, debug)
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), flush=True)
@@ -56,9 +71,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
     if verbose:
         sys.stdout.write(res.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -1027,13 +1027,24 @@ int attn_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream)
 int attn_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int a = 0, b = 0, c = 0, t = 0;
+  unsigned int a = 0, b = 0, c = 0, t = 0, dbg = 0;
   const unsigned int zero = 0;
   if ((e = cudaMemcpyFromSymbol(&a, g_prefill_status, sizeof(a))) != cudaSuccess ||
       (e = cudaMemcpyFromSymbol(&b, g_decode_status, sizeof(b))) != cudaSuccess ||
       (e = cudaMemcpyFromSymbol(&c, g_bwd_status, sizeof(c))) != cudaSuccess ||
-      (e = cudaMemcpyFromSymbol(&t, g_selftest_status, sizeof(t))) != cudaSuccess)
+      (e = cudaMemcpyFromSymbol(&t, g_selftest_status, sizeof(t))) != cudaSuccess ||
+      (e = cudaMemcpyFromSymbol(&dbg, g_debug_status, sizeof(dbg))) != cudaSuccess)
     return cuda_fail(e, "reading the device status word");
+  if (dbg) {  // debug build only: a device-side check failed
+    cudaMemcpyToSymbol(g_debug_status, &zero, sizeof(zero));
+    if ((a | b | c | t) == 0)
+      return fail(B300ATTN_ERR_INVALID,
+                  "debug build: a device-side check failed (bits 0x%x: 1 kv_len outside "
+                  "[0, max_kv_len], 2 cu_seqlens not monotone or outside [0, total_rows], "
+                  "4/8/16/32/64 a prefill item, band tile, decode split, backward tile or "
+                  "FP8 tile outside the launch)",
+                  dbg);
+  }
   if (a | b | c | t) {
     cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
     cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(zero));

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(384, 1)
   // the CTAs resident at one time share a few heads' Q and dO in L2.
   int jt, bh;
   bwd_order(blockIdx.x, nkt, p.B * p.Hkv, jt, bh);
+  if (threadIdx.x == 0) B300_DCHECK(jt >= 0 && jt < nkt && bh >= 0 && bh < p.B * p.Hkv, kDbgBwdTile);
   const int hk = bh % p.Hkv;
   const int b = bh / p.Hkv;
   const int G = p.Hq / p.Hkv;
@@ -469,6 +470,7 @@ __global__ void __launch_bounds__(384, 1)
   // from the last query tile: under a causal mask it sees the most key tiles.
   int it, bh;
   bwd_order(blockIdx.x, nqt, p.B * p.Hq, it, bh);
+  if (threadIdx.x == 0) B300_DCHECK(it >= 0 && it < nqt && bh >= 0 && bh < p.B * p.Hq, kDbgBwdTile);
   if (p.causal) it = nqt - 1 - it;
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;

@@ -72,6 +72,7 @@ __device__ __forceinline__ BandTile band_tile(const PrefillParams& p, int x, int
   const int r1 = min(t.r0 + 127, p.N - 1);
   t.jlo = max(0, t.r0 - p.window) / 128;
   t.jhi = min(p.N - 1, r1 + p.window) / 128;
+  B300_DCHECK(t.b < p.B && t.r0 < p.N && t.jlo <= t.jhi, kDbgBandTile);
   return t;
 }
 

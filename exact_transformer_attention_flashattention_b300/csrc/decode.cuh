@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
   // overlaps this grid's last CTAs instead of following them.
   grid_launch_dependents();
   int len = p.kv_len[b];
+  if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0)
+    B300_DCHECK(len >= 0 && len <= p.Lmax, kDbgKvLen);
+  if (threadIdx.x == 0)
+    B300_DCHECK(b < p.B && hq0 + GT <= p.Hq && split < p.S, kDbgDecodeSplit);
   len = min(max(len, 0), p.Lmax);
   const int key0 = split * p.chunk;
   const int nkeys = min(max(len - key0, 0), p.chunk);

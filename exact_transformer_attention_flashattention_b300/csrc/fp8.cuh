@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
     const int t = static_cast<int>(job % p.nt);
     const int h = static_cast<int>((job / p.nt) % H);
     const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * H));
+    if (tid == 0) B300_DCHECK(b < p.B, kDbgFp8Job);
     uint4 w[8];
     float m = 0.f;
 #pragma unroll
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   const int t = static_cast<int>(job % p.nt);
   const int hk = static_cast<int>((job / p.nt) % p.Hkv);
   const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * p.Hkv));
+  if (tid == 0) B300_DCHECK(b < p.B, kDbgFp8Job);
   const size_t bh = static_cast<size_t>(b) * p.Hkv + hk;
   // Transposing mapping: lane = group of 4 consecutive keys (4*lane .. 4*lane+3),
   // warp w covers 8 elements of d at w*8 and w*8 + 64.  Each thread packs the

@@ -128,6 +128,9 @@ struct PrefillItem {
 // First row and length of variable-length sequence s, clamped so that every
 // row the kernel touches lies inside [0, total_rows) whatever cu_seqlens holds.
 __device__ __forceinline__ void varlen_seq(const PrefillParams& p, int s, int& base, int& n) {
+  B300_DCHECK(p.cu_seqlens[s] >= 0 && p.cu_seqlens[s] <= p.cu_seqlens[s + 1] &&
+                  p.cu_seqlens[s + 1] <= p.total_rows,
+              kDbgCuSeqlens);
   const int a = min(max(p.cu_seqlens[s], 0), p.total_rows);
   const int e = min(max(p.cu_seqlens[s + 1], a), p.total_rows);
   base = a;
@@ -187,6 +190,10 @@ __device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p,
   }
   it.J0 = it.act[1] ? min(it.jlo[0], it.jlo[1]) : it.jlo[0];
   it.J1 = it.act[1] ? max(it.jhi[0], it.jhi[1]) : it.jhi[0];
+  B300_DCHECK(it.b >= 0 && it.b < p.num_seqs && it.h >= 0 && it.h < p.Hq && it.qb >= 0 &&
+                  (!it.act[0] || (it.jlo[0] <= it.jhi[0] && it.jhi[0] * BN < it.n)) &&
+                  (!it.act[1] || (it.jlo[1] <= it.jhi[1] && it.jhi[1] * BN < it.n)),
+              kDbgPrefillItem);
   return it;
 }
 

@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "debug.cuh"
+
 namespace b300 {
 
 // ----------------------------------------------------------------- generic

@@ -381,6 +381,14 @@ int lse_tree_combine(const float* part_m, const float* part_l, const float* part
  * B300ATTN_ERR_INVALID if the only event was a paged decode reading a
  * block_table entry outside [0, num_pages), B300ATTN_ERR_CUDA if the
  * synchronisation failed, else B300ATTN_OK.
+ *
+ * Debug build (libb300attn_debug.so, compiled with -DB300ATTN_DEBUG): the
+ * kernels also check caller data that the release build clamps (a decode
+ * kv_len entry outside [0, max_kv_len]; cu_seqlens that decrease or leave
+ * [0, total_rows]) and their own tile and index invariants.  A failed check
+ * makes this call return B300ATTN_ERR_INVALID, with the check's bits in
+ * attn_last_error(); the kernels themselves carry on with the clamped values
+ * and compute what the release build computes.
  */
 int attn_device_status(cudaStream_t stream);
 
