@@ -34,6 +34,8 @@
 // other half, as the forward does with its two query tiles.
 #pragma once
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace b300 {
@@ -356,34 +358,44 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence(us);
         reg_fence(ud);
         uint32_t pk[16], dk[16];
+        // The mask test is taken once per chunk, outside the unrolled loop, so
+        // that each version of the loop is one basic block whose eight
+        // iterations the compiler can interleave (a branch inside the loop
+        // would serialise their load -> ex2 -> pack chains).
+        auto pass = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {  // four query columns per iteration
-          const int col = 64 * wg + ch * 32 + 2 * e;
-          const float4 nl = *reinterpret_cast<const float4*>(nlse + col);
-          const float4 nd = *reinterpret_cast<const float4*>(ndv + col);
-          const float2 x0 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
-                                  sl2x2, make_float2(nl.x, nl.y));
-          const float2 x1 = ffma2(make_float2(__uint_as_float(us[2 * e + 2]), __uint_as_float(us[2 * e + 3])),
-                                  sl2x2, make_float2(nl.z, nl.w));
-          float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-          float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-          if (!full_tile) {
-            const int q = r0 + col;
-            p0.x = bwd_visible(q, key, N, causal, p.window) ? p0.x : 0.f;
-            p0.y = bwd_visible(q + 1, key, N, causal, p.window) ? p0.y : 0.f;
-            p1.x = bwd_visible(q + 2, key, N, causal, p.window) ? p1.x : 0.f;
-            p1.y = bwd_visible(q + 3, key, N, causal, p.window) ? p1.y : 0.f;
+          for (int e = 0; e < 16; e += 2) {  // four query columns per iteration
+            const int col = 64 * wg + ch * 32 + 2 * e;
+            const float4 nl = *reinterpret_cast<const float4*>(nlse + col);
+            const float4 nd = *reinterpret_cast<const float4*>(ndv + col);
+            const float2 x0 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
+                                    sl2x2, make_float2(nl.x, nl.y));
+            const float2 x1 = ffma2(make_float2(__uint_as_float(us[2 * e + 2]), __uint_as_float(us[2 * e + 3])),
+                                    sl2x2, make_float2(nl.z, nl.w));
+            float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+            float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+            if constexpr (decltype(masked)::value) {
+              const int q = r0 + col;
+              p0.x = bwd_visible(q, key, N, causal, p.window) ? p0.x : 0.f;
+              p0.y = bwd_visible(q + 1, key, N, causal, p.window) ? p0.y : 0.f;
+              p1.x = bwd_visible(q + 2, key, N, causal, p.window) ? p1.x : 0.f;
+              p1.y = bwd_visible(q + 3, key, N, causal, p.window) ? p1.y : 0.f;
+            }
+            const float2 d0 = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
+                                    make_float2(nd.x, nd.y));
+            const float2 d1 = fadd2(make_float2(__uint_as_float(ud[2 * e + 2]), __uint_as_float(ud[2 * e + 3])),
+                                    make_float2(nd.z, nd.w));
+            const float2 ds0 = fmul2(p0, d0), ds1 = fmul2(p1, d1);
+            pk[e] = pack_bf16x2(p0.x, p0.y);
+            pk[e + 1] = pack_bf16x2(p1.x, p1.y);
+            dk[e] = pack_bf16x2(ds0.x, ds0.y);
+            dk[e + 1] = pack_bf16x2(ds1.x, ds1.y);
           }
-          const float2 d0 = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
-                                  make_float2(nd.x, nd.y));
-          const float2 d1 = fadd2(make_float2(__uint_as_float(ud[2 * e + 2]), __uint_as_float(ud[2 * e + 3])),
-                                  make_float2(nd.z, nd.w));
-          const float2 ds0 = fmul2(p0, d0), ds1 = fmul2(p1, d1);
-          pk[e] = pack_bf16x2(p0.x, p0.y);
-          pk[e + 1] = pack_bf16x2(p1.x, p1.y);
-          dk[e] = pack_bf16x2(ds0.x, ds0.y);
-          dk[e + 1] = pack_bf16x2(ds1.x, ds1.y);
-        }
+        };
+        if (full_tile)
+          pass(std::false_type{});
+        else
+          pass(std::true_type{});
         tmem_st16(tS + lane_off + ch * 16, pk);
         tmem_st16(tP + lane_off + ch * 16, dk);
       }
@@ -634,21 +646,28 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence(us);
         reg_fence(ud);
         uint32_t dk[16];
+        // the mask test outside the unrolled loop (see the dK/dV kernel)
+        auto pass = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 x = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
-                                 sl2x2, nlse2);
-          float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          if (!full_tile) {
-            const int key = c0 + 64 * wg + ch * 32 + 2 * e;
-            pe.x = bwd_visible(row, key, N, causal, p.window) ? pe.x : 0.f;
-            pe.y = bwd_visible(row, key + 1, N, causal, p.window) ? pe.y : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            const float2 x = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
+                                   sl2x2, nlse2);
+            float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if constexpr (decltype(masked)::value) {
+              const int key = c0 + 64 * wg + ch * 32 + 2 * e;
+              pe.x = bwd_visible(row, key, N, causal, p.window) ? pe.x : 0.f;
+              pe.y = bwd_visible(row, key + 1, N, causal, p.window) ? pe.y : 0.f;
+            }
+            const float2 dd = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
+                                    ndrow2);
+            const float2 ds = fmul2(pe, dd);
+            dk[e] = pack_bf16x2(ds.x, ds.y);
           }
-          const float2 dd = fadd2(make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])),
-                                  ndrow2);
-          const float2 ds = fmul2(pe, dd);
-          dk[e] = pack_bf16x2(ds.x, ds.y);
-        }
+        };
+        if (full_tile)
+          pass(std::false_type{});
+        else
+          pass(std::true_type{});
         tmem_st16(tP + lane_off + ch * 16, dk);
       }
       tmem_wait_st();
