@@ -19,6 +19,8 @@
 // cores with a butterfly reduce-scatter across the lanes that share a key.
 #pragma once
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace b300 {
@@ -315,21 +317,30 @@ __global__ void __launch_bounds__(kDecThreads, (GT <= 4) ? 3 : 1)
     }
     __syncwarp();
 
-    // ---- o += p v over this group's keys
+    // ---- o += p v over this group's keys.  V rows at or past nvalid may hold
+    // anything (0 times a non-finite value is not 0), so a partial stage
+    // skips them; a full stage takes the unguarded loop, one basic block whose
+    // keys the compiler can interleave (the test is uniform over the CTA).
+    auto pv_keys = [&](auto guarded) {
 #pragma unroll
-    for (int kk = 0; kk < KPG; ++kk) {
-      const int kl = grp * KPG + kk;
-      if (wkey0 + kl < nvalid) {
-        float2 vf[4];
-        unpack8(*reinterpret_cast<const uint4*>(Vs + (wkey0 + kl) * (D * 2) + li * 16), vf);
+      for (int kk = 0; kk < KPG; ++kk) {
+        const int kl = grp * KPG + kk;
+        if (!decltype(guarded)::value || wkey0 + kl < nvalid) {
+          float2 vf[4];
+          unpack8(*reinterpret_cast<const uint4*>(Vs + (wkey0 + kl) * (D * 2) + li * 16), vf);
 #pragma unroll
-        for (int g = 0; g < GT; ++g) {
-          const float2 pg = p_w[kl * GT + g];
+          for (int g = 0; g < GT; ++g) {
+            const float2 pg = p_w[kl * GT + g];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[g][e] = ffma2(vf[e], pg, acc[g][e]);
+            for (int e = 0; e < 4; ++e) acc[g][e] = ffma2(vf[e], pg, acc[g][e]);
+          }
         }
       }
-    }
+    };
+    if (nvalid == kDecSub)
+      pv_keys(std::false_type{});
+    else
+      pv_keys(std::true_type{});
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
