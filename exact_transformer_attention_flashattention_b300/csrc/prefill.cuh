@@ -52,6 +52,14 @@ constexpr unsigned kStatusPrefillBadPage = 4096u;
 // Maximum number of sequences of one variable-length launch (the per-CTA item
 // table lives in shared memory).
 constexpr int kMaxVarlenSeqs = 4096;
+// P_i(j) V_j is issued in this many parts along the keys (32-key chunks
+// grouped evenly).  The softmax signals each part as soon as its columns of
+// P are written, so the tensor core starts O += P V on the first keys while
+// the exponentials of the last keys are still being computed.  Two parts pay
+// in FP8, where writing P (e4m3 into shared memory) is the longer pass; in
+// bf16 they measured no faster than one.
+__host__ __device__ constexpr int pv_parts(bool fp8) { return fp8 ? 2 : 1; }
+constexpr int kPvPartsMax = 2;
 
 // Two layouts share one kernel.  Dense: B sequences of N tokens,
 // q [B, N, Hq, d], LSE [B, Hq, N].  Variable length: `cu_seqlens[0..num_seqs]`
@@ -235,7 +243,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* o_full = p_full + 2;          // [2]
   uint64_t* o_empty = o_full + 2;         // [2]
   uint64_t* mma_done = o_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  constexpr int kPvParts = pv_parts(FP8);
+  static_assert(kPvParts >= 1 && kPvParts <= kPvPartsMax && 4 % kPvParts == 0,
+                "parts of the four 32-key chunks");
+  uint64_t* p_part = mma_done + 1;  // [2][kPvParts - 1]: leading parts of P_i written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_part + 2 * (kPvPartsMax - 1));
   int* table = reinterpret_cast<int*>(smem + C::TABLE_OFF);
 
   const int warp = threadIdx.x >> 5;
@@ -298,6 +310,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(mma_done, 1);
+    for (int x = 0; x < 2 * (kPvParts - 1); ++x) mbar_init(&p_part[x], 128);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -431,20 +444,27 @@ __global__ void __launch_bounds__(384, 1)
     // O_i += P_i V.  bf16: P (bf16 pairs) from tensor memory, V MN-major in
     // shared memory, 16 keys per instruction.  FP8: P (e4m3) and V^T both
     // K-major in shared memory, 32 keys per instruction.
-    auto issue_PV = [&](int i, int stage, bool accumulate) {
+    // Part `part` of kPvParts covers keys [part, part + 1) * BN / kPvParts.
+    auto issue_PV = [&](int i, int stage, bool accumulate, int part) {
       if constexpr (FP8) {
+        constexpr int KK = BN / 32 / kPvParts;
         const uint64_t a0 = dp0 + static_cast<uint64_t>((i * C::BM * BN) >> 4);
         const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 32; ++kk)
+        for (int x = 0; x < KK; ++x) {
+          const int kk = part * KK + x;
           umma_ss_f8_warp(tmem + 256 + i * D, a0 + ((kk * 32) >> 4), b0 + ((kk * 32) >> 4), idO,
                           (accumulate || kk > 0) ? 1u : 0u);
+        }
       } else {
+        constexpr int KK = BN / 16 / kPvParts;
         const uint64_t b0 = dv0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
+        for (int x = 0; x < KK; ++x) {
+          const int kk = part * KK + x;
           umma_ts_warp(tmem + 256 + i * D, tmem + i * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
                        idO, (accumulate || kk > 0) ? 1u : 0u);
+        }
       }
     };
 
@@ -500,12 +520,20 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
           if (!ok) break;
           if (it.act[i] && j >= it.jlo[i] && j <= it.jhi[i]) {
-            if (!(ok = wait(&p_full[i], pcnt[i] & 1))) break;
+            // each part of P_i once the softmax has written it; the item's
+            // first part also once the epilogue has read the previous O_i
+#pragma unroll
+            for (int part = 0; part < kPvParts && ok; ++part) {
+              uint64_t* pb = (part + 1 < kPvParts) ? &p_part[i * (kPvParts - 1) + part] : &p_full[i];
+              if (!(ok = wait(pb, pcnt[i] & 1))) break;
+              if (part == 0 && j == it.jlo[i] && ocnt[i] > 0 &&
+                  !(ok = wait(&o_empty[i], (ocnt[i] - 1) & 1)))
+                break;
+              tc_fence_after();
+              issue_PV(i, sv, j != it.jlo[i], part);
+            }
+            if (!ok) break;
             ++pcnt[i];
-            if (j == it.jlo[i] && ocnt[i] > 0 && !(ok = wait(&o_empty[i], (ocnt[i] - 1) & 1)))
-              break;
-            tc_fence_after();
-            issue_PV(i, sv, j != it.jlo[i]);
             if (j == it.jhi[i]) {
               umma_commit_warp(&o_full[i]);
               ++ocnt[i];
@@ -636,6 +664,23 @@ __global__ void __launch_bounds__(384, 1)
           l *= alpha;
         }
         const float neg_mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        // Rescale this row of O (only rows whose maximum moved; the previous
+        // P V of this tile is complete because S_i(j) was committed after
+        // it).  It runs before the first part of P is released, after which
+        // the tensor core may add into O, and after that part's exponentials,
+        // whose scores no longer need registers.
+        auto rescale_o = [&]() {
+          if (j > jlo && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t w[32];
+              tmem_ld32_wait(tO + cc * 32, w);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+              tmem_st32(tO + cc * 32, w);
+            }
+          }
+        };
         // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
         // in four packed partial sums; bf16 pairs into tensor memory, or e4m3
         // quadruples into the swizzled shared-memory P tile
@@ -676,24 +721,22 @@ __global__ void __launch_bounds__(384, 1)
           } else {
             tmem_st16(tS + q * 16, pk);
           }
+          // a leading part of P is complete: the tensor core may start on it
+          constexpr int QP = 4 / kPvParts;  // 32-key chunks per part
+          if ((q + 1) % QP == 0 && q + 1 < 4) {
+            if (q + 1 == QP) rescale_o();
+            if constexpr (FP8) fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_part[i * (kPvParts - 1) + (q + 1) / QP - 1]);
+          }
         }
+        if constexpr (kPvParts == 1) rescale_o();
         if constexpr (FP8) fence_proxy_async_smem();  // P tile -> tensor-core operand
         {
           const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
           const float2 t = fadd2(a, b2);
           l += t.x + t.y;
-        }
-        // Rescale this row of O (only rows whose maximum moved; the previous
-        // P V of this tile is complete because S_i(j) was committed after it).
-        if (j > jlo && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t w[32];
-            tmem_ld32_wait(tO + cc * 32, w);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-            tmem_st32(tO + cc * 32, w);
-          }
         }
         tmem_wait_st();
         tc_fence_before();
