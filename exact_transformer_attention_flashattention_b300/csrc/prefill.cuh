@@ -103,11 +103,9 @@ struct PrefillCfg {
   // bf16 the K/V ring would have to shrink to three stages, so one Q buffer
   // is kept there.
   static constexpr int QBUF = (D == 128 && !FP8) ? 1 : 2;
-  static constexpr int STAGES = FP8 ? 6 : ((D == 128) ? 4 : 8);
+  static constexpr int STAGES = FP8 ? 8 : ((D == 128) ? 4 : 8);
   static constexpr int RING_OFF = QBUF * 2 * TILE_BYTES;
-  // FP8: the e4m3 P tile of each Q tile (128 rows x 128 keys, 128-byte swizzle)
-  static constexpr int P_OFF = RING_OFF + STAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = P_OFF + (FP8 ? 2 * BM * BN : 0);
+  static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
   // + barriers and the TMEM address (512 B), the variable-length item table
   // (kMaxVarlenSeqs + 1 ints), alignment slack
   static constexpr int TABLE_OFF = BAR_OFF + 512;
@@ -212,9 +210,10 @@ __device__ __forceinline__ PrefillItem prefill_item_info(const PrefillParams& p,
 // but one byte per element, V stored transposed ([B, Hkv, d, Np], so that the
 // PV product reads it K-major), tcgen05 kind::f8f6f4 with 32 elements of K
 // per instruction.  The softmax multiplies the raw scores by
-// scale * 2^-(e_Q + e_K) of the tile pair, writes P rounded to e4m3 into a
-// swizzled shared-memory tile (the A operand of PV), and the epilogue divides
-// by l and by 2^e_V.  The lazy rescale keeps P <= 2^8 < 448, inside e4m3.
+// scale * 2^-(e_Q + e_K) of the tile pair, writes P rounded to e4m3 into
+// tensor memory over the first 32 columns of its S (four keys to a column,
+// the A operand of PV), and the epilogue divides by l and by 2^e_V.  The lazy
+// rescale keeps P <= 2^8 < 448, inside e4m3.
 //
 // PAGED selects K and V gathered from a page pool through a block table
 // (dense layout of q, bf16): each 128-key tile is two 64-row TMA boxes, each
@@ -418,7 +417,6 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(smem_u32(sRing), 16, 1024);
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sRing), BN * 128, 1024);
-    const uint64_t dp0 = smem_desc_sw128(smem_u32(smem + C::P_OFF), 16, 1024);
     uint32_t pcnt[2] = {0u, 0u};  // p_full phases consumed, per Q tile
     uint32_t ocnt[2] = {0u, 0u};  // items in which Q tile i was active
     auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -441,19 +439,19 @@ __global__ void __launch_bounds__(384, 1)
       }
       umma_commit_warp(&s_full[i]);
     };
-    // O_i += P_i V.  bf16: P (bf16 pairs) from tensor memory, V MN-major in
-    // shared memory, 16 keys per instruction.  FP8: P (e4m3) and V^T both
-    // K-major in shared memory, 32 keys per instruction.
+    // O_i += P_i V.  P from tensor memory (bf16 pairs or e4m3 quadruples in
+    // the first columns of S_i).  bf16: V MN-major in shared memory, 16 keys
+    // per instruction.  FP8: V^T K-major in shared memory, 32 keys per
+    // instruction.
     // Part `part` of kPvParts covers keys [part, part + 1) * BN / kPvParts.
     auto issue_PV = [&](int i, int stage, bool accumulate, int part) {
       if constexpr (FP8) {
         constexpr int KK = BN / 32 / kPvParts;
-        const uint64_t a0 = dp0 + static_cast<uint64_t>((i * C::BM * BN) >> 4);
         const uint64_t b0 = dk0 + static_cast<uint64_t>((stage * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int x = 0; x < KK; ++x) {
           const int kk = part * KK + x;
-          umma_ss_f8_warp(tmem + 256 + i * D, a0 + ((kk * 32) >> 4), b0 + ((kk * 32) >> 4), idO,
+          umma_ts_f8_warp(tmem + 256 + i * D, tmem + i * 128 + kk * 8, b0 + ((kk * 32) >> 4), idO,
                           (accumulate || kk > 0) ? 1u : 0u);
         }
       } else {
@@ -682,8 +680,8 @@ __global__ void __launch_bounds__(384, 1)
           }
         };
         // P = 2^(s*scale*log2e - m) on column pairs (packed f32x2 FMA), row sum
-        // in four packed partial sums; bf16 pairs into tensor memory, or e4m3
-        // quadruples into the swizzled shared-memory P tile
+        // in four packed partial sums; bf16 pairs or e4m3 quadruples into the
+        // first columns of S in tensor memory
         const float2 sl2x2 = make_float2(c, c);
         const float2 nmu2 = make_float2(neg_mu, neg_mu);
         float2 lacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -706,18 +704,12 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           if constexpr (FP8) {
-            // keys 32q .. 32q+31 are 16-byte chunks 2q and 2q+1 of this row;
-            // chunk k of row r sits at position k ^ (r mod 8) (128-byte swizzle)
-            const uint32_t prow = smem_u32(smem + C::P_OFF) + i * (C::BM * BN) + (r >> 3) * 1024 +
-                                  (r & 7) * 128;
+            // keys 32q .. 32q+31: columns 8q .. 8q+7, four keys to a column
+            uint32_t p8[8];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const float* f = pv + 16 * h2;
-              st_shared_v4(prow + (((2 * q + h2) ^ (r & 7)) << 4),
-                           pack_e4m3x4(f[0], f[1], f[2], f[3]), pack_e4m3x4(f[4], f[5], f[6], f[7]),
-                           pack_e4m3x4(f[8], f[9], f[10], f[11]),
-                           pack_e4m3x4(f[12], f[13], f[14], f[15]));
-            }
+            for (int e = 0; e < 8; ++e)
+              p8[e] = pack_e4m3x4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+            tmem_st8(tS + q * 8, p8);
           } else {
             tmem_st16(tS + q * 16, pk);
           }
@@ -725,14 +717,12 @@ __global__ void __launch_bounds__(384, 1)
           constexpr int QP = 4 / kPvParts;  // 32-key chunks per part
           if ((q + 1) % QP == 0 && q + 1 < 4) {
             if (q + 1 == QP) rescale_o();
-            if constexpr (FP8) fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_part[i * (kPvParts - 1) + (q + 1) / QP - 1]);
           }
         }
         if constexpr (kPvParts == 1) rescale_o();
-        if constexpr (FP8) fence_proxy_async_smem();  // P tile -> tensor-core operand
         {
           const float2 a = fadd2(lacc[0], lacc[1]), b2 = fadd2(lacc[2], lacc[3]);
           const float2 t = fadd2(a, b2);

@@ -108,13 +108,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, fl
   return r;
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (tensor-core operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -342,6 +335,20 @@ __device__ __forceinline__ void umma_ss_f8_warp(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem] with e4m3 operands (kind::f8f6f4, 32
+// elements of K per instruction, four to a 32-bit tensor-memory column, the
+// lowest byte first); warp-wide, one elected lane issues.
+__device__ __forceinline__ void umma_ts_f8_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled tile.
 // [0,14) start>>4, [16,30) leading byte offset>>4, [32,46) stride byte offset>>4,
 // [46,48) version 1, [61,64) layout 2 = 128B swizzle.
@@ -405,6 +412,14 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 }
 
 // 32 lanes x 16 columns of 32-bit into tensor memory (completion: tmem_wait_st).
+// 32 lanes x 8 columns of 32-bit into tensor memory (completion: tmem_wait_st).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
