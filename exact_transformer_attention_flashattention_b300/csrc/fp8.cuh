@@ -13,7 +13,9 @@
 //
 // Two launches: fp8_vamax_kernel writes the absolute maximum of every
 // 128-key tile of V; fp8_quantize_kernel then runs one CTA per 128-row tile of
-// Q, of K and of V (V reduces its head's tile maxima first).
+// V, of Q and of K (V reduces its head's tile maxima first).  The V tiles
+// come first, in the reverse of the order the maximum kernel read them, so
+// that their second read finds V still in L2.
 #pragma once
 
 #include "ptx.cuh"
@@ -103,10 +105,11 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   __shared__ __align__(16) uint8_t sT[D * 128];  // V tile transposed: [d][128 keys]
   const int tid = threadIdx.x;
   const long long nq = static_cast<long long>(p.B) * p.Hq * p.nt;
-  const long long nk = static_cast<long long>(p.B) * p.Hkv * p.nt;
+  const long long nk = static_cast<long long>(p.B) * p.Hkv * p.nt;  // = the number of V tiles
   long long job = blockIdx.x;
 
-  if (job < nq + nk) {
+  if (job >= nk) {
+    job -= nk;
     // ------------------------------------------------------------- Q or K tile
     const bool isq = job < nq;
     if (!isq) job -= nq;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   }
 
   // ----------------------------------------------------------------- V tile
-  job -= nq + nk;
+  job = nk - 1 - job;
   const int t = static_cast<int>(job % p.nt);
   const int hk = static_cast<int>((job / p.nt) % p.Hkv);
   const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * p.Hkv));
