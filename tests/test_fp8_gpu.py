@@ -131,6 +131,24 @@ def test_fwd_fp8_matches_oracle(fa, case):
     _check_attention(O, L, ref["q"], ref["k"], ref["v"], causal, window, scale, bf16_out=bf16_out)
 
 
+def test_fwd_fp8_rescale_every_tile(fa):
+    """Key rows of tile t scaled by 1 + 4t and scale 0.5: each key tile raises
+    most rows' maximum by far more than the 2^8 rescale threshold, so the
+    running O is rescaled on every tile (before the first half of P·V of that
+    tile may add into it)."""
+    B, H, N, d = 1, 2, 640, 128
+    q, k, v = prefill_inputs(B, H, H, N, d, seed=21)
+    ramp = (1.0 + 4.0 * (torch.arange(N) // 128)).view(1, N, 1, 1)
+    k = (k.float() * ramp).bfloat16()
+    for causal in (False, True):
+        qz = fa.attn_fp8_quantize(q.cuda(), k.cuda(), v.cuda())
+        O, L = fa.attn_fwd_fp8(qz, causal=causal, scale=0.5, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert fa.device_status() == 0
+        ref = f8.quantize_inputs(q, k, v)
+        _check_attention(O, L, ref["q"], ref["k"], ref["v"], causal, -1, 0.5, bf16_out=False)
+
+
 def test_fp8_full_size_sampled(fa):
     """The causal N=4096, d=128 workload shape (B=4, 16 heads) in the launch
     configuration the benchmark times: quantisation bit-exact in full, attention
