@@ -13,9 +13,7 @@
 //
 // Two launches: fp8_vamax_kernel writes the absolute maximum of every
 // 128-key tile of V; fp8_quantize_kernel then runs one CTA per 128-row tile of
-// V, of Q and of K (V reduces its head's tile maxima first).  The V tiles
-// come first, in the reverse of the order the maximum kernel read them, so
-// that their second read finds V still in L2.
+// Q, of K and of V (V reduces its head's tile maxima first).
 #pragma once
 
 #include "ptx.cuh"
@@ -105,11 +103,10 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   __shared__ __align__(16) uint8_t sT[D * 128];  // V tile transposed: [d][128 keys]
   const int tid = threadIdx.x;
   const long long nq = static_cast<long long>(p.B) * p.Hq * p.nt;
-  const long long nk = static_cast<long long>(p.B) * p.Hkv * p.nt;  // = the number of V tiles
+  const long long nk = static_cast<long long>(p.B) * p.Hkv * p.nt;
   long long job = blockIdx.x;
 
-  if (job >= nk) {
-    job -= nk;
+  if (job < nq + nk) {
     // ------------------------------------------------------------- Q or K tile
     const bool isq = job < nq;
     if (!isq) job -= nq;
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   }
 
   // ----------------------------------------------------------------- V tile
-  job = nk - 1 - job;
+  job -= nq + nk;
   const int t = static_cast<int>(job % p.nt);
   const int hk = static_cast<int>((job / p.nt) % p.Hkv);
   const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * p.Hkv));
