@@ -473,7 +473,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = ring_empty + STAGES;  // [2] S and dP of key half w in tensor memory
   uint64_t* p_ready = s_full + 2;          // [2] dS of half w written (128 threads)
   uint64_t* acc_done = p_ready + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* qin_full = acc_done + 1;       // Q_i, dO_i copied into tensor memory (256 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qin_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
@@ -504,6 +505,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&p_ready[w], C::EW_THREADS / 2);
     }
     mbar_init(acc_done, 1);
+    mbar_init(qin_full, C::EW_THREADS);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -515,8 +517,10 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // tensor memory: key half w (64 keys) has S at [128w, 128w+64) and dP at
-  // [128w+64, 128w+128); dQ [256,256+D)
+  // [128w+64, 128w+128); dQ [256,256+D); Q_i and dO_i as bf16 pairs (the A
+  // operands of S and dP) at [384, 384+D/2) and [448, 448+D/2)
   const uint32_t tQ = tmem + 256;
+  const uint32_t tQin = tmem + 384, tDOin = tmem + 448;
 
   if (warp == 0) {
     // ================================================================ producer
@@ -551,8 +555,6 @@ __global__ void __launch_bounds__(384, 1)
     // ================================================================ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 64, false);  // 128 queries x 64 keys
     const uint32_t idO = idesc_bf16_f32(128, D, true);
-    const uint64_t dQ0 = smem_desc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
-    const uint64_t dDO0 = smem_desc_sw128(smem_u32(smem + L::DO_OFF), 16, 1024);
     const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 16, 1024);
     const uint64_t dRmn = smem_desc_sw128(smem_u32(smem + L::RING_OFF), 128 * 128, 1024);
     auto wait = [&](uint64_t* bar, uint32_t parity, unsigned site) {
@@ -560,18 +562,21 @@ __global__ void __launch_bounds__(384, 1)
     };
     // S_w = Q K_w^T and dP_w = dO V_w^T for key half w: rows 64w.. of the
     // stage's K / V tiles (8 KB into each 128-byte-wide block)
+    // Q and dO are read from tensor memory (8 columns = 16 elements of d per
+    // instruction), so that shared memory serves only the K / V half (2 KB
+    // per instruction instead of 6 KB with Q and dO there too).
     auto issue_sdp = [&](int w, int s) {
       const uint64_t kK = dR0 + static_cast<uint64_t>((s * L::STAGE_BYTES + w * 64 * 128) >> 4);
       const uint64_t vK = kK + static_cast<uint64_t>(C::TILE_BYTES >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tmem + 128 * w, dQ0 + off, kK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ts_warp(tmem + 128 * w, tQin + kk * 8, kK + off, idS, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
-        umma_ss_warp(tmem + 128 * w + 64, dDO0 + off, vK + off, idS, kk > 0 ? 1u : 0u);
+        umma_ts_warp(tmem + 128 * w + 64, tDOin + kk * 8, vK + off, idS, kk > 0 ? 1u : 0u);
       }
       umma_commit_warp(&s_full[w]);
     };
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(384, 1)
         umma_ts_warp(tQ, tmem + 128 * w + 64 + k4 * 8, kMN + (((4 * w + k4) * 16 * 128) >> 4),
                      idO, (!first || k4 > 0) ? 1u : 0u);
     };
-    bool ok = wait(q_full, 0, kStatusBwdMma);
+    bool ok = wait(qin_full, 0, kStatusBwdMma);
     if (ok && nsteps > 0 && (ok = wait(&ring_full[0], 0, kStatusBwdMma))) {
       tc_fence_after();
       issue_sdp(0, 0);
@@ -624,7 +629,29 @@ __global__ void __launch_bounds__(384, 1)
     const float ndrow = (row < N) ? -p.dvec[vi] : 0.f;
     const float2 sl2x2 = make_float2(sl2, sl2), nlse2 = make_float2(nlse, nlse);
     const float2 ndrow2 = make_float2(ndrow, ndrow);
-    bool ok = true;
+    // Q_i (warpgroup 0) or dO_i (warpgroup 1) into tensor memory: this
+    // thread's row, un-swizzled from the TMA tile (16-byte unit k of row r
+    // at position k ^ (r mod 8)), as bf16 pairs in d order
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, &g_bwd_status, kStatusBwdCompute));
+    if (ok) {
+      const uint8_t* src = smem + (wg ? L::DO_OFF : L::Q_OFF) + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < C::DCH; ++cc) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(src + cc * (128 * 128) + ((k ^ (r & 7)) << 4));
+          w[4 * k] = v4.x;
+          w[4 * k + 1] = v4.y;
+          w[4 * k + 2] = v4.z;
+          w[4 * k + 3] = v4.w;
+        }
+        tmem_st32((wg ? tDOin : tQin) + lane_off + cc * 32, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qin_full);
+    }
     for (int t = 0; t < nsteps && ok; ++t) {
       const int c0 = (jlo + t) * 128;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], t & 1, &g_bwd_status,
