@@ -444,15 +444,21 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ---------------------------------------------------------------- dQ
+// Three K/V stages (K tile, V tile each).  Q_i and dO_i land in stage 0's
+// space and are copied into tensor memory at the start; step t loads stage
+// (t + 1) mod 3, so stage 0 is first reused at step 2, once the copy is done.
 template <int D>
 struct DqSmem {
   using C = BwdCfg<D>;
+  static constexpr int STAGES = 3;
   static constexpr int Q_OFF = 0;
   static constexpr int DO_OFF = C::TILE_BYTES;
-  static constexpr int RING_OFF = 2 * C::TILE_BYTES;  // stage: K tile, V tile
+  static constexpr int RING_OFF = 0;
   static constexpr int STAGE_BYTES = 2 * C::TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + C::STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE_BYTES;
   static constexpr int BYTES = BAR_OFF + 256 + 1024;
+  // ring stage of step t; the stage's uses before step t number t / STAGES
+  static __device__ __forceinline__ int stage(int t) { return (t + 1) % STAGES; }
 };
 
 template <int D>
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(384, 1)
                   const BwdParams p) {
   using C = BwdCfg<D>;
   using L = DqSmem<D>;
-  constexpr int STAGES = C::STAGES;
+  constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -533,10 +539,14 @@ __global__ void __launch_bounds__(384, 1)
       int t = 0;
       bool ok = true;
       for (; t < nsteps && ok; ++t) {
-        const int s = t % STAGES;
+        const int s = L::stage(t);
         if (t >= STAGES &&
             !(ok = mbar_wait(&ring_empty[s], ((t / STAGES) - 1) & 1, &g_bwd_status,
                              kStatusBwdProducer)))
+          break;
+        // stage 0 holds Q_i and dO_i until they are in tensor memory
+        if (t == STAGES - 1 &&
+            !(ok = mbar_wait(qin_full, 0, &g_bwd_status, kStatusBwdProducer)))
           break;
         const int c0 = (jlo + t) * 128;
         uint8_t* st = smem + L::RING_OFF + s * L::STAGE_BYTES;
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       for (int u = max(0, t - STAGES); u < t; ++u)
-        mbar_wait(&ring_full[u % STAGES], (u / STAGES) & 1, &g_bwd_status, kStatusBwdProducer);
+        mbar_wait(&ring_full[L::stage(u)], (u / STAGES) & 1, &g_bwd_status, kStatusBwdProducer);
       mbar_wait(q_full, 0, &g_bwd_status, kStatusBwdProducer);
     }
   } else if (warp == 1) {
@@ -590,13 +600,13 @@ __global__ void __launch_bounds__(384, 1)
                      idO, (!first || k4 > 0) ? 1u : 0u);
     };
     bool ok = wait(qin_full, 0, kStatusBwdMma);
-    if (ok && nsteps > 0 && (ok = wait(&ring_full[0], 0, kStatusBwdMma))) {
+    if (ok && nsteps > 0 && (ok = wait(&ring_full[L::stage(0)], 0, kStatusBwdMma))) {
       tc_fence_after();
-      issue_sdp(0, 0);
-      issue_sdp(1, 0);
+      issue_sdp(0, L::stage(0));
+      issue_sdp(1, L::stage(0));
     }
     for (int t = 0; t < nsteps && ok; ++t) {
-      const int s = t % STAGES, s1 = (t + 1) % STAGES;
+      const int s = L::stage(t), s1 = L::stage(t + 1);
       const bool has_next = t + 1 < nsteps;
       if (!(ok = wait(&p_ready[0], t & 1, kStatusBwdMmaP))) break;
       tc_fence_after();
