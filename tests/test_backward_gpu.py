@@ -43,6 +43,9 @@ CASES = [
     (1, 2, 1, 200, 64, False, 50),
     (1, 4, 4, 640, 128, True, 128),
     (1, 8, 2, 384, 128, False, -1),
+    # d = 64 with five key tiles per query tile: the dQ kernel's K/V ring
+    # wraps into the stage where Q and dO arrived
+    (1, 2, 2, 640, 64, False, -1),
 ]
 
 
