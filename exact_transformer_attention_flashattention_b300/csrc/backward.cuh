@@ -127,7 +127,8 @@ struct DkdvSmem {
   static constexpr int V_OFF = C::TILE_BYTES;
   static constexpr int RING_OFF = 2 * C::TILE_BYTES;              // stage: Q tile, dO tile
   static constexpr int STAGE_BYTES = 2 * C::TILE_BYTES;
-  static constexpr int VEC_OFF = RING_OFF + C::STAGES * STAGE_BYTES;  // [2 slots][lse2, dvec][128] f32
+  // [2 slots][2 warpgroups][-LSE2, -D][64 queries] f32
+  static constexpr int VEC_OFF = RING_OFF + C::STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * 128 * 4;
   static constexpr int BYTES = BAR_OFF + 256 + 1024;  // barriers + TMEM address, alignment slack
 };
@@ -151,8 +152,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = ring_empty + STAGES;  // [2] S^T and dP^T of query half w in tensor memory
   uint64_t* p_ready = s_full + 2;          // [2] P^T, dS^T of half w written (128 threads)
   uint64_t* acc_done = p_ready + 2;        // every MMA done
-  uint64_t* vec_full = acc_done + 1;       // [2] per-query vectors staged (256 threads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 2);
+  uint64_t* vec_full = acc_done + 1;       // [2 slots][2 warpgroups] vectors staged (128 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
@@ -190,8 +191,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&p_ready[w], C::EW_THREADS / 2);
     }
     mbar_init(acc_done, 1);
-    mbar_init(&vec_full[0], C::EW_THREADS);
-    mbar_init(&vec_full[1], C::EW_THREADS);
+    for (int x = 0; x < 4; ++x) mbar_init(&vec_full[x], C::EW_THREADS / 2);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -316,28 +316,30 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     const bool causal = p.causal != 0;
-    // this thread's entry of step t's per-query vector, negated: -LSE (base 2)
-    // from warpgroup 1, -D from warpgroup 2; loaded one step ahead
+    // this thread's entry of step t's per-query vectors for its warpgroup's
+    // 64 queries, negated: -LSE (base 2) from threads 0-63, -D from threads
+    // 64-127; loaded one step ahead
     auto vec_entry = [&](int t) -> float {
-      const int q = (ilo + t % nq) * 128 + r;
+      const int q = (ilo + t % nq) * 128 + 64 * wg + (r & 63);
       const size_t vi = (static_cast<size_t>(b) * p.Hq + hk * G + t / nq) * N + q;
       if (q >= N) return 0.f;
-      return wg == 0 ? -p.lse[vi] * kLog2e : -p.dvec[vi];
+      return r < 64 ? -p.lse[vi] * kLog2e : -p.dvec[vi];
     };
     float v_next = nsteps > 0 ? vec_entry(0) : 0.f;
     bool ok = true;
     for (int t = 0; t < nsteps && ok; ++t) {
       const int r0 = (ilo + t % nq) * 128;
-      // the step's vectors are staged in shared memory (two slots; a slot is
-      // rewritten only after every element-wise thread has arrived for the
-      // step in between, i.e. finished reading it)
-      float* nlse = vec + (t & 1) * 256;
-      float* ndv = nlse + 128;
-      (wg == 0 ? nlse : ndv)[r] = v_next;
+      // the step's vectors are staged in shared memory, per warpgroup (two
+      // slots; a slot is rewritten only after every thread of the warpgroup
+      // has arrived for the step in between, i.e. finished reading it), so
+      // the two warpgroups never wait for each other
+      float* nlse = vec + ((t & 1) * 2 + wg) * 128;
+      float* ndv = nlse + 64;
+      (r < 64 ? nlse : ndv)[r & 63] = v_next;
       if (t + 1 < nsteps) v_next = vec_entry(t + 1);
-      mbar_arrive(&vec_full[t & 1]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&vec_full[t & 1], (t >> 1) & 1, &g_bwd_status,
-                                             kStatusBwdVec));
+      uint64_t* vf = &vec_full[(t & 1) * 2 + wg];
+      mbar_arrive(vf);
+      ok = __all_sync(0xffffffffu, mbar_wait(vf, (t >> 1) & 1, &g_bwd_status, kStatusBwdVec));
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], t & 1, &g_bwd_status,
                                              kStatusBwdCompute));
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(384, 1)
         auto pass = [&](auto masked) {
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {  // four query columns per iteration
-            const int col = 64 * wg + ch * 32 + 2 * e;
+            const int col = ch * 32 + 2 * e;  // within the warpgroup's 64 queries
             const float4 nl = *reinterpret_cast<const float4*>(nlse + col);
             const float4 nd = *reinterpret_cast<const float4*>(ndv + col);
             const float2 x0 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(384, 1)
             float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
             float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
             if constexpr (decltype(masked)::value) {
-              const int q = r0 + col;
+              const int q = r0 + 64 * wg + col;
               p0.x = bwd_visible(q, key, N, causal, p.window) ? p0.x : 0.f;
               p0.y = bwd_visible(q + 1, key, N, causal, p.window) ? p0.y : 0.f;
               p1.x = bwd_visible(q + 2, key, N, causal, p.window) ? p1.x : 0.f;
