@@ -206,6 +206,12 @@ __global__ void __launch_bounds__(384, 1)
   // at [128w+64, 128w+128); dV [256,256+D)  dK [256+D,256+2D)
   const uint32_t tV = tmem + 256, tK = tmem + 256 + D;
 
+  // Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup
+  // 0 (producer, MMA issuer, allocator, idle) gives back to 88 and the two
+  // element-wise warpgroups take 208, so that a step's four tensor-memory
+  // loads fit in registers together: 128 x 88 + 256 x 208 = 64512.
+  if (warp < 4) {
+  setmaxnreg_dec<88>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
@@ -305,7 +311,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     umma_commit_warp(acc_done);
     wait(acc_done, 0, kStatusBwdMma);
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<208>();
     // ================================================================ element-wise
     const int quarter = warp & 3;
     const int wg = (warp - 4) >> 2;     // query half: columns 64*wg .. 64*wg+63 of the tile
@@ -349,16 +357,25 @@ __global__ void __launch_bounds__(384, 1)
                              (!causal || r0 >= c0 + 127) &&
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
-      // two chunks of 32 columns; chunk ch's bf16 pairs go to columns
-      // [16ch, 16ch+16) of the same array, already read by then
-#pragma unroll 1
+      // two chunks of 32 columns, all four loads in flight behind one wait;
+      // chunk ch's bf16 pairs go to columns [16ch, 16ch+16) of the same
+      // array, read before any store
+      uint32_t us2[2][32], ud2[2][32];
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(tS + lane_off + ch * 32, us);
-        tmem_ld32(tP + lane_off + ch * 32, ud);
-        tmem_wait_ld();
-        reg_fence(us);
-        reg_fence(ud);
+        tmem_ld32(tS + lane_off + ch * 32, us2[ch]);
+        tmem_ld32(tP + lane_off + ch * 32, ud2[ch]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        reg_fence(us2[ch]);
+        reg_fence(ud2[ch]);
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const uint32_t (&us)[32] = us2[ch];
+        const uint32_t (&ud)[32] = ud2[ch];
         uint32_t pk[16], dk[16];
         // The mask test is taken once per chunk, outside the unrolled loop, so
         // that each version of the loop is one basic block whose eight
