@@ -413,7 +413,10 @@ int launch_backward(const void* q, const void* k, const void* v, const BwdParams
   if ((rc = set_smem(bwd_dkdv_kernel<D>, DkdvSmem<D>::BYTES)) != B300ATTN_OK) return rc;
   if ((rc = set_smem(bwd_dq_kernel<D>, DqSmem<D>::BYTES)) != B300ATTN_OK) return rc;
   const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
-  bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  {
+    constexpr long long per = bwd_preprocess_rows_per_cta<D>();
+    bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + per - 1) / per), 256, 0, stream>>>(p);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   const long long ntile = (p.N + 127) / 128;

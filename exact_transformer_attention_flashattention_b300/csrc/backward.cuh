@@ -59,29 +59,75 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
-// One warp per (b, i, h) row; rows are numbered in the [B, N, Hq] order of O.
+// Rows are numbered in the [B, N, Hq] order of O.  A row is read by D/8 lanes,
+// 16 bytes of dO (and of a bf16 O) each; a warp covers 256/D rows per pass and
+// keeps kPrePasses passes of loads in flight before it reduces any of them.
+constexpr int kPrePasses = 4;
+template <int D>
+constexpr long long bwd_preprocess_rows_per_cta() { return 8LL * (256 / D) * kPrePasses; }
+
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
+  float acc = bf16lo_to_f32(a.x) * bf16lo_to_f32(b.x);
+  acc = fmaf(bf16hi_to_f32(a.x), bf16hi_to_f32(b.x), acc);
+  acc = fmaf(bf16lo_to_f32(a.y), bf16lo_to_f32(b.y), acc);
+  acc = fmaf(bf16hi_to_f32(a.y), bf16hi_to_f32(b.y), acc);
+  acc = fmaf(bf16lo_to_f32(a.z), bf16lo_to_f32(b.z), acc);
+  acc = fmaf(bf16hi_to_f32(a.z), bf16hi_to_f32(b.z), acc);
+  acc = fmaf(bf16lo_to_f32(a.w), bf16lo_to_f32(b.w), acc);
+  acc = fmaf(bf16hi_to_f32(a.w), bf16hi_to_f32(b.w), acc);
+  return acc;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int LPR = D / 8;      // lanes per row
+  constexpr int RPW = 32 / LPR;   // rows per warp and pass
   const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, l = lane % LPR;
   const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
-  if (row >= rows) return;
-  float acc = 0.f;
-  const __nv_bfloat16* dOr = p.dO + row * D;
+  const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW * kPrePasses;
+  uint4 g[kPrePasses], o[kPrePasses], o2[kPrePasses];
 #pragma unroll
-  for (int e = lane; e < D; e += 32) {
-    const float o = p.o_f32 ? static_cast<const float*>(p.o)[row * D + e]
-                            : __bfloat162float(static_cast<const __nv_bfloat16*>(p.o)[row * D + e]);
-    acc = fmaf(__bfloat162float(dOr[e]), o, acc);
+  for (int u = 0; u < kPrePasses; ++u) {
+    const long long row = row0 + u * RPW + sub;
+    g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows) {
+      g[u] = reinterpret_cast<const uint4*>(p.dO + row * D)[l];
+      if (p.o_f32) {
+        const uint4* of = reinterpret_cast<const uint4*>(static_cast<const float*>(p.o) + row * D);
+        o[u] = of[2 * l];
+        o2[u] = of[2 * l + 1];
+      } else {
+        o[u] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + row * D)[l];
+      }
+    }
   }
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) {
-    const int h = static_cast<int>(row % p.Hq);
-    const long long bi = row / p.Hq;
-    const int i = static_cast<int>(bi % p.N);
-    const int b = static_cast<int>(bi / p.N);
-    p.dvec[(static_cast<long long>(b) * p.Hq + h) * p.N + i] = acc;
+  for (int u = 0; u < kPrePasses; ++u) {
+    float acc;
+    if (p.o_f32) {
+      const uint4 a = o[u], b = o2[u];
+      acc = bf16lo_to_f32(g[u].x) * __uint_as_float(a.x);
+      acc = fmaf(bf16hi_to_f32(g[u].x), __uint_as_float(a.y), acc);
+      acc = fmaf(bf16lo_to_f32(g[u].y), __uint_as_float(a.z), acc);
+      acc = fmaf(bf16hi_to_f32(g[u].y), __uint_as_float(a.w), acc);
+      acc = fmaf(bf16lo_to_f32(g[u].z), __uint_as_float(b.x), acc);
+      acc = fmaf(bf16hi_to_f32(g[u].z), __uint_as_float(b.y), acc);
+      acc = fmaf(bf16lo_to_f32(g[u].w), __uint_as_float(b.z), acc);
+      acc = fmaf(bf16hi_to_f32(g[u].w), __uint_as_float(b.w), acc);
+    } else {
+      acc = dot8_bf16(g[u], o[u]);
+    }
+#pragma unroll
+    for (int m = LPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    const long long row = row0 + u * RPW + sub;
+    if (l == 0 && row < rows) {
+      const int h = static_cast<int>(row % p.Hq);
+      const long long bi = row / p.Hq;
+      const int i = static_cast<int>(bi % p.N);
+      const int b = static_cast<int>(bi / p.N);
+      p.dvec[(static_cast<long long>(b) * p.Hq + h) * p.N + i] = acc;
+    }
   }
 }
 
