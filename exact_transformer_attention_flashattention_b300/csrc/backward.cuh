@@ -593,6 +593,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tQ = tmem + 256;
   const uint32_t tQin = tmem + 384, tDOin = tmem + 448;
 
+  // Register split as in the dK/dV kernel: 128 x 88 + 256 x 208 = 384 x 168.
+  if (warp < 4) {
+  setmaxnreg_dec<88>();
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
@@ -689,7 +692,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     umma_commit_warp(acc_done);
     wait(acc_done, 0, kStatusBwdMma);
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<208>();
     // ================================================================ element-wise
     const int quarter = warp & 3;
     const int wg = (warp - 4) >> 2;     // key half: columns 64*wg .. 64*wg+63 of the tile
@@ -737,16 +742,25 @@ __global__ void __launch_bounds__(384, 1)
                              (!causal || r0 >= c0 + 127) &&
                              (p.window < 0 || (r0 + 127 - c0 <= p.window &&
                                                (causal || c0 + 127 - r0 <= p.window)));
-      // two chunks of 32 columns; chunk ch's bf16 pairs go to columns
-      // [16ch, 16ch+16) of the half's dP, already read by then
-#pragma unroll 1
+      // two chunks of 32 columns, all four loads behind one wait; chunk ch's
+      // bf16 pairs go to columns [16ch, 16ch+16) of the half's dP, read
+      // before any store
+      uint32_t us2[2][32], ud2[2][32];
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(tS + lane_off + ch * 32, us);
-        tmem_ld32(tP + lane_off + ch * 32, ud);
-        tmem_wait_ld();
-        reg_fence(us);
-        reg_fence(ud);
+        tmem_ld32(tS + lane_off + ch * 32, us2[ch]);
+        tmem_ld32(tP + lane_off + ch * 32, ud2[ch]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        reg_fence(us2[ch]);
+        reg_fence(ud2[ch]);
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const uint32_t (&us)[32] = us2[ch];
+        const uint32_t (&ud)[32] = ud2[ch];
         uint32_t dk[16];
         // the mask test outside the unrolled loop (see the dK/dV kernel)
         auto pass = [&](auto masked) {
