@@ -13,12 +13,29 @@
 //
 // Two launches: fp8_vamax_kernel writes the absolute maximum of every
 // 128-key tile of V; fp8_quantize_kernel then runs one CTA per 128-row tile of
-// Q, of K and of V (V reduces its head's tile maxima first).
+// Q, of K and of V (V reduces its head's tile maxima first).  A quantisation
+// CTA brings its tile into shared memory with one bulk copy per row, so its
+// bytes are in flight without holding registers and more CTAs fit on an SM.
 #pragma once
 
+#include "prefill.cuh"  // g_prefill_status, which also reports this file's bounded wait
 #include "ptx.cuh"
 
 namespace b300 {
+
+// bit of g_prefill_status: the quantisation kernel gave up waiting for its tile
+constexpr unsigned kStatusFp8Stage = 1u << 20;
+
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completion signalled on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 struct Fp8QuantParams {
   const __nv_bfloat16* q;  // [B, N, Hq, D]
@@ -100,8 +117,26 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
     fp8_quantize_kernel(const Fp8QuantParams p) {
   static_assert(D == 128, "tile mappings assume d = 128");
   __shared__ float red[kFp8QuantThreads / 32];
-  __shared__ __align__(16) uint8_t sT[D * 128];  // V tile transposed: [d][128 keys]
+  // the tile's rows (row r at r * 2D bytes); a V tile's transpose, [d][128
+  // keys] of e4m3, reuses its first 16 KB once the rows are in registers
+  __shared__ __align__(128) uint8_t sX[128 * D * 2];
+  __shared__ uint64_t xbar;
+  uint8_t* sT = sX;
   const int tid = threadIdx.x;
+  // Rows t*128 .. of head h of x into sX: one 2D-byte bulk copy per row
+  // inside the sequence; false if the copies did not land in time.
+  auto stage = [&](const __nv_bfloat16* x, int b, int h, int H, int t) -> bool {
+    const int nrows = min(128, p.N - t * 128);
+    if (tid == 0) {
+      mbar_init(&xbar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(nrows) * D * 2);
+    }
+    __syncthreads();
+    if (tid < nrows)
+      bulk_load(sX + tid * D * 2, tile_row_ptr<D>(x, b, h, H, p.N, t * 128 + tid), D * 2, &xbar);
+    return mbar_wait(&xbar, 0, &g_prefill_status, kStatusFp8Stage);
+  };
   const long long nq = static_cast<long long>(p.B) * p.Hq * p.nt;
   const long long nk = static_cast<long long>(p.B) * p.Hkv * p.nt;
   long long job = blockIdx.x;
@@ -118,14 +153,14 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
     const int h = static_cast<int>((job / p.nt) % H);
     const int b = static_cast<int>(job / (static_cast<long long>(p.nt) * H));
     if (tid == 0) B300_DCHECK(b < p.B, kDbgFp8Job);
-    uint4 w[8];
+    stage(x, b, h, H, t);
+    // the rows are read twice from shared memory, for the maximum and for
+    // the codes, so that no register holds them across the reduction
     float m = 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int row = t * 128 + u * 16 + tid / 16;
-      w[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (row < p.N) w[u] = tile_row_ptr<D>(x, b, h, H, p.N, row)[tid % 16];
-      m = absmax8(w[u], m);
+      const int rr = u * 16 + tid / 16;  // row within the tile
+      if (t * 128 + rr < p.N) m = absmax8(reinterpret_cast<const uint4*>(sX + rr * D * 2)[tid % 16], m);
     }
     m = block_max256(m, red);
     const int e = fp8_scale_exponent(m);
@@ -133,13 +168,15 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
     if (tid == 0) ex[(static_cast<size_t>(b) * H + h) * p.nt + t] = e;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int row = t * 128 + u * 16 + tid / 16;
+      const int rr = u * 16 + tid / 16;
+      const int row = t * 128 + rr;
       if (row >= p.N) continue;
+      const uint4 w = reinterpret_cast<const uint4*>(sX + rr * D * 2)[tid % 16];
       uint2 o;
-      o.x = pack_e4m3x4(bf16lo_to_f32(w[u].x) * s, bf16hi_to_f32(w[u].x) * s,
-                        bf16lo_to_f32(w[u].y) * s, bf16hi_to_f32(w[u].y) * s);
-      o.y = pack_e4m3x4(bf16lo_to_f32(w[u].z) * s, bf16hi_to_f32(w[u].z) * s,
-                        bf16lo_to_f32(w[u].w) * s, bf16hi_to_f32(w[u].w) * s);
+      o.x = pack_e4m3x4(bf16lo_to_f32(w.x) * s, bf16hi_to_f32(w.x) * s,
+                        bf16lo_to_f32(w.y) * s, bf16hi_to_f32(w.y) * s);
+      o.y = pack_e4m3x4(bf16lo_to_f32(w.z) * s, bf16hi_to_f32(w.z) * s,
+                        bf16lo_to_f32(w.w) * s, bf16hi_to_f32(w.w) * s);
       reinterpret_cast<uint2*>(y + ((static_cast<size_t>(b) * p.N + row) * H + h) * D)[tid % 16] = o;
     }
     return;
@@ -158,21 +195,23 @@ __global__ void __launch_bounds__(kFp8QuantThreads)
   // loads are issued before the head's maximum is reduced, so both are in
   // flight together.
   const int rg = tid & 31, cg = tid >> 5;
+  float m = 0.f;
+  for (int u = tid; u < p.nt; u += kFp8QuantThreads) m = fmaxf(m, p.v_tile_amax[bh * p.nt + u]);
+  stage(p.v, b, hk, p.Hkv, t);
+  m = block_max256(m, red);
+  const int e = fp8_scale_exponent(m);
+  const float s = pow2i(e);
+  if (tid == 0 && t == 0) p.v_exp[bh] = e;
   uint4 wt[2][4];
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row = t * 128 + 4 * rg + i;
+      const int rr = 4 * rg + i;  // row within the tile
       wt[pass][i] = make_uint4(0u, 0u, 0u, 0u);
-      if (row < p.N) wt[pass][i] = tile_row_ptr<D>(p.v, b, hk, p.Hkv, p.N, row)[cg + 8 * pass];
+      if (t * 128 + rr < p.N) wt[pass][i] = reinterpret_cast<const uint4*>(sX + rr * D * 2)[cg + 8 * pass];
     }
-  float m = 0.f;
-  for (int u = tid; u < p.nt; u += kFp8QuantThreads) m = fmaxf(m, p.v_tile_amax[bh * p.nt + u]);
-  m = block_max256(m, red);
-  const int e = fp8_scale_exponent(m);
-  const float s = pow2i(e);
-  if (tid == 0 && t == 0) p.v_exp[bh] = e;
+  __syncthreads();  // every row read before the transpose overwrites them
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     const int c8 = cg + 8 * pass;  // 16-byte column of d
