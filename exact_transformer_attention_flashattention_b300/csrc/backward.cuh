@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_ready = s_full + 2;          // [2] P^T, dS^T of half w written (128 threads)
   uint64_t* acc_done = p_ready + 2;        // every MMA done
   uint64_t* vec_full = acc_done + 1;       // [2 slots][2 warpgroups] vectors staged (128 threads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 4);
+  uint64_t* p_half = vec_full + 4;        // [2] first 32 queries of half w written (128 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(acc_done, 1);
     for (int x = 0; x < 4; ++x) mbar_init(&vec_full[x], C::EW_THREADS / 2);
+    for (int w = 0; w < 2; ++w) mbar_init(&p_half[w], C::EW_THREADS / 2);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -319,18 +321,35 @@ __global__ void __launch_bounds__(384, 1)
     };
     // dV += P^T_w dO_w and dK += dS^T_w Q_w: A from tensor memory (the half's
     // bf16 pairs, in the first 32 columns of its S^T / dP^T), B the stage's
-    // dO / Q rows of the half read MN-major, 16 queries per instruction
-    auto issue_grad = [&](int w, int s, bool first) {
+    // dO / Q rows of the half read MN-major, 16 queries per instruction.
+    // Part 0 covers the half's first 32 queries (its first element-wise
+    // chunk), part 1 the other 32.
+    auto issue_grad = [&](int w, int s, bool first, int part) {
       const uint64_t qMN = dRmn + static_cast<uint64_t>((s * L::STAGE_BYTES) >> 4);
       const uint64_t doMN = qMN + static_cast<uint64_t>(C::TILE_BYTES >> 4);
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4)
+      for (int x = 0; x < 2; ++x) {
+        const int k4 = 2 * part + x;
         umma_ts_warp(tV, tmem + 128 * w + k4 * 8, doMN + (((4 * w + k4) * 16 * 128) >> 4), idO,
                      (!first || k4 > 0) ? 1u : 0u);
+      }
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4)
+      for (int x = 0; x < 2; ++x) {
+        const int k4 = 2 * part + x;
         umma_ts_warp(tK, tmem + 128 * w + 64 + k4 * 8, qMN + (((4 * w + k4) * 16 * 128) >> 4),
                      idO, (!first || k4 > 0) ? 1u : 0u);
+      }
+    };
+    // both parts of half w's gradients, each once the element-wise pass has
+    // written its chunk
+    auto grads = [&](int w, int s, bool first, uint32_t parity) {
+      if (!wait(&p_half[w], parity, kStatusBwdMmaP)) return false;
+      tc_fence_after();
+      issue_grad(w, s, first, 0);
+      if (!wait(&p_ready[w], parity, kStatusBwdMmaP)) return false;
+      tc_fence_after();
+      issue_grad(w, s, first, 1);
+      return true;
     };
     bool ok = wait(kv_full, 0, kStatusBwdMma);
     if (ok && nsteps > 0 && (ok = wait(&ring_full[0], 0, kStatusBwdMma))) {
@@ -341,17 +360,13 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < nsteps && ok; ++t) {
       const int s = t % STAGES, s1 = (t + 1) % STAGES;
       const bool has_next = t + 1 < nsteps;
-      if (!(ok = wait(&p_ready[0], t & 1, kStatusBwdMmaP))) break;
-      tc_fence_after();
-      issue_grad(0, s, t == 0);
+      if (!(ok = grads(0, s, t == 0, t & 1))) break;
       if (has_next) {
         if (!(ok = wait(&ring_full[s1], ((t + 1) / STAGES) & 1, kStatusBwdMma))) break;
         tc_fence_after();
         issue_sdp(0, s1);
       }
-      if (!(ok = wait(&p_ready[1], t & 1, kStatusBwdMmaP))) break;
-      tc_fence_after();
-      issue_grad(1, s, false);
+      if (!(ok = grads(1, s, false, t & 1))) break;
       umma_commit_warp(&ring_empty[s]);
       if (has_next) issue_sdp(1, s1);
     }
@@ -463,6 +478,13 @@ __global__ void __launch_bounds__(384, 1)
           pass(std::true_type{});
         tmem_st16(tS + lane_off + ch * 16, pk);
         tmem_st16(tP + lane_off + ch * 16, dk);
+        // the first 32 queries' P^T and dS^T are in place: their gradient
+        // MMAs may start while the second chunk is computed
+        if (ch == 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_half[wg]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
