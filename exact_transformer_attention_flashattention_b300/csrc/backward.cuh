@@ -15,8 +15,9 @@
 //                          bf16, then dV += P^T dO and dK += dS^T Q with P^T / dS^T read
 //                          from tensor memory.
 //   bwd_dq_kernel          one CTA per (sequence, query head, 128-query tile): Q_i, dO_i
-//                          stay; K_j, V_j stream; S = Q K^T, dP = dO V^T, dS back to
-//                          tensor memory, dQ += dS K.
+//                          stay, copied into tensor memory as the A operands of S and
+//                          dP; K_j, V_j stream through three stages; S = Q K^T,
+//                          dP = dO V^T, dS back to tensor memory, dQ += dS K.
 // Splitting dQ from dK/dV recomputes S and dP once more but needs no atomics and
 // gives a deterministic result.
 //
